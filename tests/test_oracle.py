@@ -1,0 +1,267 @@
+"""Pins for the double-precision oracle (CPU only).
+
+Each test checks the oracle against something other than itself: a closed
+form, an invariant of the DFT, a brute-force definition written differently
+(2D double sums, circular convolution), or numpy's pocketfft rfft2/irfft2, which
+computes exactly the orthonormal irfft2(Z, s=(H, W)) of the layer's
+definition.  Together they fail on a dropped term, a wrong sign or index, a
+transposed operand, a wrong scale or a wrong retained-row order.
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+RNG = np.random.default_rng(12345)
+
+
+def kept_rows(H, m1):
+    return list(range(m1)) + list(range(H - m1, H))
+
+
+def numpy_layer(x, w, m1, m2):
+    """The layer through numpy's FFT library (independent of the oracle)."""
+    B, Cin, H, W = x.shape
+    F = np.fft.rfft2(x, norm="ortho")
+    rows = kept_rows(H, m1)
+    Z = np.einsum("bixy,ioxy->boxy", F[:, :, rows, :m2], w)
+    full = np.zeros((B, w.shape[1], H, W // 2 + 1), dtype=complex)
+    full[:, :, rows, :m2] = Z
+    return np.fft.irfft2(full, s=(H, W), norm="ortho")
+
+
+def rand_w(Cin, Cout, m1, m2):
+    return RNG.standard_normal((Cin, Cout, 2 * m1, m2)) + 1j * RNG.standard_normal(
+        (Cin, Cout, 2 * m1, m2))
+
+
+# ---------------------------------------------------------------- forward ---
+
+@pytest.mark.parametrize("H,W,h0,w0", [(8, 8, 3, 5), (16, 4, 0, 1), (4, 32, 2, 31)])
+def test_forward_delta_is_flat_phase(H, W, h0, w0):
+    x = np.zeros((1, 1, H, W))
+    x[0, 0, h0, w0] = 1.0
+    m1, m2 = H // 2, W // 2 + 1
+    X = oracle.forward_modes(x, m1, m2)[0, 0]
+    for r, k1 in enumerate(kept_rows(H, m1)):
+        for k2 in range(m2):
+            ref = np.exp(-2j * np.pi * (k1 * h0 / H + k2 * w0 / W)) / np.sqrt(H * W)
+            assert abs(X[r, k2] - ref) < 1e-14
+    assert np.allclose(np.abs(X), 1 / np.sqrt(H * W), atol=1e-15)
+
+
+def test_forward_constant_is_dc_only():
+    H, W, c = 16, 8, 2.5
+    x = np.full((1, 1, H, W), c)
+    X = oracle.forward_modes(x, 4, 3)[0, 0]
+    assert abs(X[0, 0] - np.sqrt(H * W) * c) < 1e-12
+    X[0, 0] = 0
+    assert np.abs(X).max() < 1e-12
+
+
+@pytest.mark.parametrize("p,q", [(2, 0), (1, 3), (-3, 2)])
+def test_forward_single_cosine(p, q):
+    H, W = 16, 16
+    h = np.arange(H)[:, None]
+    w = np.arange(W)[None, :]
+    x = np.cos(2 * np.pi * (p * h / H + q * w / W))[None, None]
+    m1, m2 = 4, 5
+    X = oracle.forward_modes(x, m1, m2)[0, 0]
+    expect = np.zeros_like(X)
+    rows = kept_rows(H, m1)
+    half = np.sqrt(H * W) / 2
+    for (kp, kq) in [(p % H, q), ((-p) % H, -q)]:
+        if 0 <= kq < m2 and kp in rows:
+            expect[rows.index(kp), kq] += half
+    assert np.abs(X - expect).max() < 1e-12
+
+
+@pytest.mark.parametrize("H,W", [(8, 8), (4, 16), (16, 2)])
+def test_forward_parseval_full_modes(H, W):
+    x = RNG.standard_normal((2, 3, H, W))
+    X = oracle.forward_modes(x, H // 2, W // 2 + 1)
+    # half spectrum: bins 1..W/2-1 stand for themselves and their mirrors
+    wgt = np.full(W // 2 + 1, 2.0)
+    wgt[0] = 1.0
+    wgt[W // 2] = 1.0
+    energy_X = (np.abs(X) ** 2 * wgt).sum(axis=(2, 3))
+    energy_x = (x ** 2).sum(axis=(2, 3))
+    assert np.allclose(energy_X, energy_x, rtol=1e-13)
+
+
+def test_forward_brute_force_2d_sum():
+    H, W, m1, m2 = 4, 8, 1, 3
+    x = RNG.standard_normal((1, 2, H, W))
+    X = oracle.forward_modes(x, m1, m2)
+    for c in range(2):
+        for r, k1 in enumerate(kept_rows(H, m1)):
+            for k2 in range(m2):
+                s = 0j
+                for h in range(H):
+                    for w in range(W):
+                        s += x[0, c, h, w] * np.exp(-2j * np.pi * (k1 * h / H + k2 * w / W))
+                assert abs(X[0, c, r, k2] - s / np.sqrt(H * W)) < 1e-13
+
+
+@pytest.mark.parametrize("H,W,m1,m2", [(16, 16, 4, 4), (8, 32, 4, 17), (32, 8, 3, 2)])
+def test_forward_matches_numpy_rfft2(H, W, m1, m2):
+    x = RNG.standard_normal((2, 3, H, W))
+    X = oracle.forward_modes(x, m1, m2)
+    F = np.fft.rfft2(x, norm="ortho")[:, :, kept_rows(H, m1), :m2]
+    assert np.abs(X - F).max() < 1e-13
+
+
+# -------------------------------------------------------------------- mix ---
+
+def test_mix_matches_numpy_complex_matmul():
+    B, Cin, Cout, nm = 3, 5, 4, 7
+    X = RNG.standard_normal((B, Cin, nm)) + 1j * RNG.standard_normal((B, Cin, nm))
+    w = RNG.standard_normal((Cin, Cout, nm)) + 1j * RNG.standard_normal((Cin, Cout, nm))
+    Z = oracle.mix_modes(X, w)
+    for m in range(nm):
+        assert np.abs(Z[:, :, m] - X[:, :, m] @ w[:, :, m]).max() < 1e-13
+
+
+def test_mix_not_transposed():
+    # Cin != Cout and B != Cin: a transposed operand would not even type-check
+    X = np.zeros((2, 3, 1), complex)
+    X[1, 2, 0] = 1j
+    w = np.zeros((3, 5, 1), complex)
+    w[2, 4, 0] = 2 + 1j
+    Z = oracle.mix_modes(X, w)
+    expect = np.zeros((2, 5, 1), complex)
+    expect[1, 4, 0] = 1j * (2 + 1j)
+    assert np.abs(Z - expect).max() == 0
+
+
+# ---------------------------------------------------------------- inverse ---
+
+@pytest.mark.parametrize("H,W,m1,m2", [(16, 16, 4, 4), (8, 32, 4, 17), (32, 8, 3, 2),
+                                       (16, 16, 8, 9), (2, 2, 1, 2)])
+def test_inverse_matches_numpy_irfft2(H, W, m1, m2):
+    Z = RNG.standard_normal((2, 3, 2 * m1, m2)) + 1j * RNG.standard_normal((2, 3, 2 * m1, m2))
+    y = oracle.inverse_modes(Z, H, W)
+    full = np.zeros((2, 3, H, W // 2 + 1), complex)
+    full[:, :, kept_rows(H, m1), :m2] = Z
+    assert np.abs(y - np.fft.irfft2(full, s=(H, W), norm="ortho")).max() < 1e-13
+
+
+def test_inverse_discards_imaginary_dc_and_nyquist():
+    H, W = 8, 8
+    Z = np.zeros((1, 1, 8, 5), complex)
+    Z[0, 0, 0, 0] = 3j          # k1 = 0, k2 = 0: purely imaginary DC
+    Z[0, 0, 0, 4] = -2j         # k1 = 0, k2 = W/2: purely imaginary Nyquist
+    y = oracle.inverse_modes(Z, H, W)
+    assert np.abs(y).max() < 1e-15
+
+
+def test_inverse_at_matches_full():
+    H, W, m1, m2 = 16, 8, 3, 4
+    Z = RNG.standard_normal((2, 3, 2 * m1, m2)) + 1j * RNG.standard_normal((2, 3, 2 * m1, m2))
+    y = oracle.inverse_modes(Z, H, W)
+    idx = np.array([[0, 0, 0, 0], [1, 2, 15, 7], [1, 0, 9, 3], [0, 1, 4, 6]])
+    assert np.abs(oracle.inverse_modes_at(Z, H, W, idx) - y[tuple(idx.T)]).max() < 1e-14
+
+
+# ------------------------------------------------------------------ layer ---
+
+@pytest.mark.parametrize("B,Cin,Cout,H,W,m1,m2", [
+    (2, 4, 4, 16, 16, 4, 4),
+    (1, 3, 5, 8, 32, 2, 17),
+    (3, 2, 1, 32, 8, 16, 5),
+    (1, 1, 1, 2, 2, 1, 2),
+    (2, 6, 3, 16, 4, 1, 1),
+])
+def test_layer_matches_numpy(B, Cin, Cout, H, W, m1, m2):
+    x = RNG.standard_normal((B, Cin, H, W))
+    w = rand_w(Cin, Cout, m1, m2)
+    y = oracle.spectral_conv2d(x, w, m1, m2)
+    assert np.abs(y - numpy_layer(x, w, m1, m2)).max() < 1e-12 * max(1, np.abs(y).max())
+
+
+@pytest.mark.parametrize("H,W", [(8, 8), (16, 4), (4, 16)])
+def test_identity_weights_full_modes_give_identity(H, W):
+    C = 3
+    m1, m2 = H // 2, W // 2 + 1
+    w = np.zeros((C, C, 2 * m1, m2), complex)
+    for i in range(C):
+        w[i, i] = 1.0
+    x = RNG.standard_normal((2, C, H, W))
+    y = oracle.spectral_conv2d(x, w, m1, m2)
+    assert np.abs(y - x).max() < 1e-13
+
+
+@pytest.mark.parametrize("H,W", [(8, 8), (4, 16)])
+def test_convolution_theorem(H, W):
+    """Cin = Cout = 1, all modes, w = unnormalised DFT of g: y = x (*) g (circular)."""
+    x = RNG.standard_normal((1, 1, H, W))
+    g = RNG.standard_normal((H, W))
+    G = np.zeros((H, W), complex)
+    hh = np.arange(H)[:, None]
+    ww = np.arange(W)[None, :]
+    for k1 in range(H):
+        for k2 in range(W):
+            G[k1, k2] = (g * np.exp(-2j * np.pi * (k1 * hh / H + k2 * ww / W))).sum()
+    m1, m2 = H // 2, W // 2 + 1
+    w = G[kept_rows(H, m1), :m2][None, None]
+    y = oracle.spectral_conv2d(x, w, m1, m2)[0, 0]
+    conv = np.zeros((H, W))
+    for h in range(H):
+        for wv in range(W):
+            s = 0.0
+            for a in range(H):
+                for b in range(W):
+                    s += x[0, 0, a, b] * g[(h - a) % H, (wv - b) % W]
+            conv[h, wv] = s
+    assert np.abs(y - conv).max() < 1e-12
+
+
+def test_shift_equivariance_truncated():
+    B, C, H, W, m1, m2 = 1, 2, 16, 8, 3, 3
+    x = RNG.standard_normal((B, C, H, W))
+    w = rand_w(C, C, m1, m2)
+    y = oracle.spectral_conv2d(x, w, m1, m2)
+    ys = oracle.spectral_conv2d(np.roll(x, (5, 3), axis=(2, 3)), w, m1, m2)
+    assert np.abs(ys - np.roll(y, (5, 3), axis=(2, 3))).max() < 1e-12
+
+
+def test_linearity_in_x_and_w():
+    B, C, H, W, m1, m2 = 2, 3, 8, 8, 2, 3
+    x1, x2 = RNG.standard_normal((2, B, C, H, W))
+    w1, w2 = rand_w(C, C, m1, m2), rand_w(C, C, m1, m2)
+    a, b = 0.7, -1.3
+    f = oracle.spectral_conv2d
+    assert np.abs(f(a * x1 + b * x2, w1, m1, m2) - a * f(x1, w1, m1, m2)
+                  - b * f(x2, w1, m1, m2)).max() < 1e-12
+    assert np.abs(f(x1, a * w1 + b * w2, m1, m2) - a * f(x1, w1, m1, m2)
+                  - b * f(x1, w2, m1, m2)).max() < 1e-12
+
+
+def test_zero_input_zero_output():
+    w = rand_w(2, 2, 2, 2)
+    y = oracle.spectral_conv2d(np.zeros((1, 2, 8, 8)), w, 2, 2)
+    assert np.abs(y).max() == 0
+
+
+def test_truncation_is_not_idempotent():
+    """The retained row set keeps k1 = H - m1 but not its mirror m1, so the
+    identity-weight layer with truncation is not a projection (reading c.4)."""
+    H, W, m1, m2, C = 8, 8, 2, 2, 1
+    w = np.ones((C, C, 2 * m1, m2), complex)
+    x = RNG.standard_normal((1, C, H, W))
+    y1 = oracle.spectral_conv2d(x, w, m1, m2)
+    y2 = oracle.spectral_conv2d(y1, w, m1, m2)
+    assert np.abs(y2 - y1).max() > 1e-3
+
+
+@pytest.mark.parametrize("args", [
+    (0, 1, 8, 8, 2, 2), (1, 1, 8, 8, 5, 2), (1, 1, 8, 8, 2, 6), (1, 1, 12, 8, 2, 2),
+    (1, 1, 8, 8, 0, 2), (1, 1, 1, 8, 1, 2)])
+def test_invalid_shapes_rejected(args):
+    B, C, H, W, m1, m2 = args
+    x = np.zeros((max(B, 1), C, H, W))
+    with pytest.raises((ValueError, AssertionError)):
+        if B == 0:
+            oracle.forward_modes(np.zeros((0, C, H, W)), m1, m2)
+        else:
+            oracle.forward_modes(x, m1, m2)
