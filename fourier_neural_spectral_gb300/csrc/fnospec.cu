@@ -1,0 +1,388 @@
+// fnospec.cu -- host side of libfnospec: argument validation, plans, twiddle
+// tables, workspace layout, the one-shot plan cache and the device error word.
+// The declarations and their contracts are in include/fnospec.h.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int kMaxN = 4096;
+
+bool is_pow2(int v) { return v >= 1 && (v & (v - 1)) == 0; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+fno_status_t validate_shape(int B, int Cin, int Cout, int H, int W, int m1, int m2) {
+    if (B < 1 || Cin < 1 || Cout < 1 || H < 1 || W < 1 || m1 < 1 || m2 < 1)
+        return FNO_ERR_INVALID_ARG;
+    if (2LL * m1 > H || (long long)m2 > W / 2 + 1) return FNO_ERR_INVALID_ARG;
+    if (!is_pow2(H) || !is_pow2(W) || H < 2 || W < 2 || H > kMaxN || W > kMaxN)
+        return FNO_ERR_UNSUPPORTED;
+    const long long lim = (1LL << 31) - 1;
+    if ((long long)B * Cin * H * W > lim || (long long)B * Cout * H * W > lim ||
+        (long long)Cin * Cout * 2 * m1 * m2 > lim)
+        return FNO_ERR_UNSUPPORTED;
+    if ((long long)B * Cin > 65535 * 1024LL || (long long)B * Cout > 65535 * 1024LL)
+        return FNO_ERR_UNSUPPORTED;
+    return FNO_OK;
+}
+
+// A pointer the kernels can dereference: device or managed memory, or host
+// memory that is registered/pinned and mapped (the GPU reaches it through UVA).
+// Unregistered host memory would fault the GPU, so it is rejected here.
+fno_status_t check_ptr(const void* p, bool required) {
+    if (!p) return required ? FNO_ERR_INVALID_ARG : FNO_OK;
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return FNO_ERR_INVALID_ARG;
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error
+        return FNO_ERR_INVALID_ARG;
+    }
+    if (attr.type == cudaMemoryTypeUnregistered) return FNO_ERR_INVALID_ARG;
+    if (attr.type == cudaMemoryTypeHost && attr.devicePointer == nullptr) return FNO_ERR_INVALID_ARG;
+    return FNO_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const char* pa = static_cast<const char*>(a);
+    const char* pb = static_cast<const char*>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+fno_status_t check_device(const fno_plan_s* p) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FNO_ERR_CUDA;
+    return dev == p->device ? FNO_OK : FNO_ERR_INVALID_ARG;
+}
+
+// e^{+2 pi i j / N} for j in [0, N), evaluated in double and rounded once.
+std::vector<float2> twiddles(int N) {
+    std::vector<float2> t(N);
+    const double two_pi = 6.283185307179586476925286766559005768;
+    for (int j = 0; j < N; ++j) {
+        const double a = two_pi * (double)j / (double)N;
+        t[j] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+    return t;
+}
+
+size_t x_bytes(const fno_plan_s* p) { return 4ull * p->B * p->Cin * p->H * p->W; }
+size_t y_bytes(const fno_plan_s* p) { return 4ull * p->B * p->Cout * p->H * p->W; }
+size_t w_bytes(const fno_plan_s* p) { return 8ull * p->Cin * p->Cout * p->nm; }
+size_t X_bytes(const fno_plan_s* p) { return 8ull * p->B * p->Cin * p->nm; }
+size_t Z_bytes(const fno_plan_s* p) { return 8ull * p->B * p->Cout * p->nm; }
+
+fno_status_t check_ws(const fno_plan_s* p, const void* ws, size_t ws_bytes) {
+    if (ws_bytes < p->ws_bytes) return FNO_ERR_WORKSPACE;
+    if (p->ws_bytes == 0) return FNO_OK;
+    return check_ptr(ws, true);
+}
+
+void set_kernel(fno_plan_s* p, int k, const char* name, size_t bytes, size_t flops) {
+    std::snprintf(p->kernels[k].name, sizeof(p->kernels[k].name), "%s", name);
+    p->kernels[k].bytes = bytes;
+    p->kernels[k].flops = flops;
+}
+
+double fft_flops(double L) { return 5.0 * L * std::log2(L); }
+
+// Kernel list of the shape-generic path (stages_generic.cu + mix_fma.cu).
+void describe_generic(fno_plan_s* p) {
+    const size_t Pi = (size_t)p->B * p->Cin, Po = (size_t)p->B * p->Cout;
+    const size_t Ti = 8ull * Pi * p->H * p->m2, To = 8ull * Po * p->H * p->m2;
+    set_kernel(p, 0, "fwd_rows", x_bytes(p) + Ti, (size_t)(fft_flops(p->W) * Pi * p->H / 2));
+    set_kernel(p, 1, "fwd_cols", Ti + X_bytes(p), (size_t)(fft_flops(p->H) * Pi * p->m2));
+    set_kernel(p, 2, "mix_fma", X_bytes(p) + w_bytes(p) + Z_bytes(p),
+               8ull * p->B * p->Cin * p->Cout * p->nm);
+    set_kernel(p, 3, "inv_cols", Z_bytes(p) + To, (size_t)(fft_flops(p->H) * Po * p->m2));
+    set_kernel(p, 4, "inv_rows", To + y_bytes(p), (size_t)(fft_flops(p->W) * Po * p->H / 2));
+    p->launches = 5;
+}
+
+fno_status_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return FNO_OK;
+    return FNO_ERR_CUDA;
+}
+
+std::once_flag g_init_once;
+cudaError_t g_init_err = cudaSuccess;
+
+}  // namespace
+
+extern "C" {
+
+const char* fno_status_string(fno_status_t s) {
+    switch (s) {
+        case FNO_OK: return "FNO_OK";
+        case FNO_ERR_INVALID_ARG: return "FNO_ERR_INVALID_ARG: invalid argument";
+        case FNO_ERR_UNSUPPORTED: return "FNO_ERR_UNSUPPORTED: shape or precision not supported";
+        case FNO_ERR_CUDA: return "FNO_ERR_CUDA: CUDA runtime error";
+        case FNO_ERR_WORKSPACE: return "FNO_ERR_WORKSPACE: workspace too small";
+        case FNO_ERR_TIMEOUT: return "FNO_ERR_TIMEOUT: device-side wait timed out";
+        case FNO_ERR_DEVICE: return "FNO_ERR_DEVICE: kernel reported an internal error";
+    }
+    return "unknown fno_status_t";
+}
+
+fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, int W, int m1,
+                             int m2, fno_precision_t prec) {
+    if (!out) return FNO_ERR_INVALID_ARG;
+    *out = nullptr;
+    fno_status_t st = validate_shape(B, Cin, Cout, H, W, m1, m2);
+    if (st != FNO_OK) return st;
+    if (prec != FNO_PREC_FP32 && prec != FNO_PREC_TF32 && prec != FNO_PREC_3XTF32)
+        return FNO_ERR_INVALID_ARG;
+    if (prec != FNO_PREC_FP32) return FNO_ERR_UNSUPPORTED;
+
+    std::call_once(g_init_once, [] {
+        g_init_err = stages_generic_init();
+        if (g_init_err == cudaSuccess) g_init_err = mix_init();
+    });
+    if (g_init_err != cudaSuccess) return FNO_ERR_CUDA;
+
+    fno_plan_s* p = new fno_plan_s();
+    std::memset(p, 0, sizeof(*p));
+    p->B = B; p->Cin = Cin; p->Cout = Cout; p->H = H; p->W = W; p->m1 = m1; p->m2 = m2;
+    p->nm = 2 * m1 * m2;
+    p->prec = prec;
+    p->scale = (float)(1.0 / std::sqrt((double)H * (double)W));
+    if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return FNO_ERR_CUDA; }
+
+    // workspace: X | Z | T
+    size_t off = 0;
+    p->off_X = off; off = align_up(off + X_bytes(p), 256);
+    p->off_Z = off; off = align_up(off + Z_bytes(p), 256);
+    p->off_T = off;
+    const size_t planes = (size_t)B * (Cin > Cout ? Cin : Cout);
+    off = align_up(off + 8ull * planes * H * m2, 256);
+    p->ws_bytes = off;
+    describe_generic(p);
+    std::snprintf(p->desc, sizeof(p->desc),
+                  "generic: rows-fft(W=%d)|cols-fft(H=%d)|mix-fma|icols-fft|irows-fft, fp32", W, H);
+
+    std::vector<float2> th = twiddles(H), tw = twiddles(W);
+    cudaError_t e = cudaMalloc(&p->tw_h, sizeof(float2) * H);
+    if (e == cudaSuccess) e = cudaMalloc(&p->tw_w, sizeof(float2) * W);
+    if (e == cudaSuccess) e = cudaMalloc(&p->err, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemcpy(p->tw_h, th.data(), sizeof(float2) * H, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(p->tw_w, tw.data(), sizeof(float2) * W, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(p->err, 0, sizeof(unsigned));
+    if (e != cudaSuccess) {
+        fno_plan_destroy(p);
+        return FNO_ERR_CUDA;
+    }
+    *out = p;
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_workspace_size(fno_plan_t p, size_t* bytes) {
+    if (!p || !bytes) return FNO_ERR_INVALID_ARG;
+    *bytes = p->ws_bytes;
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_launch_count(fno_plan_t p, int* n) {
+    if (!p || !n) return FNO_ERR_INVALID_ARG;
+    *n = p->launches;
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_kernel_info(fno_plan_t p, int index, char* name, size_t name_len,
+                                  size_t* bytes, size_t* flops) {
+    if (!p || index < 0 || index >= p->launches) return FNO_ERR_INVALID_ARG;
+    if (name && name_len) std::snprintf(name, name_len, "%s", p->kernels[index].name);
+    if (bytes) *bytes = p->kernels[index].bytes;
+    if (flops) *flops = p->kernels[index].flops;
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_record_events(fno_plan_t p, cudaEvent_t* events, int count) {
+    if (!p) return FNO_ERR_INVALID_ARG;
+    if (!events) {
+        p->events = nullptr;
+        p->nevents = 0;
+        return FNO_OK;
+    }
+    if (count != p->launches + 1) return FNO_ERR_INVALID_ARG;
+    p->events = events;
+    p->nevents = count;
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_describe(fno_plan_t p, char* buf, size_t len) {
+    if (!p || !buf || len == 0) return FNO_ERR_INVALID_ARG;
+    std::snprintf(buf, len, "%s", p->desc);
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_destroy(fno_plan_t p) {
+    if (!p) return FNO_OK;
+    if (p->tw_h) cudaFree(p->tw_h);
+    if (p->tw_w) cudaFree(p->tw_w);
+    if (p->err) cudaFree(p->err);
+    delete p;
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_execute(fno_plan_t p, const float* x, const void* w, float* y, void* ws,
+                              size_t ws_bytes, cudaStream_t s) {
+    if (!p) return FNO_ERR_INVALID_ARG;
+    fno_status_t st;
+    if ((st = check_device(p)) != FNO_OK) return st;
+    if ((st = check_ptr(x, true)) != FNO_OK) return st;
+    if ((st = check_ptr(w, true)) != FNO_OK) return st;
+    if ((st = check_ptr(y, true)) != FNO_OK) return st;
+    if ((st = check_ws(p, ws, ws_bytes)) != FNO_OK) return st;
+    if (overlaps(y, y_bytes(p), x, x_bytes(p)) || overlaps(y, y_bytes(p), w, w_bytes(p)))
+        return FNO_ERR_INVALID_ARG;
+    if (p->ws_bytes && (overlaps(ws, p->ws_bytes, x, x_bytes(p)) ||
+                        overlaps(ws, p->ws_bytes, y, y_bytes(p)) ||
+                        overlaps(ws, p->ws_bytes, w, w_bytes(p))))
+        return FNO_ERR_INVALID_ARG;
+    char* base = static_cast<char*>(ws);
+    float2* X = reinterpret_cast<float2*>(base + p->off_X);
+    float2* Z = reinterpret_cast<float2*>(base + p->off_Z);
+    float2* T = reinterpret_cast<float2*>(base + p->off_T);
+    fno_launch_ctx ctx;
+    ctx.events = p->events;
+    ctx.count = p->nevents;
+    cudaError_t e = ctx.mark(s);
+    if (e == cudaSuccess) e = launch_forward_modes(*p, x, X, T, s, &ctx);
+    if (e == cudaSuccess) e = launch_mix_modes(*p, X, static_cast<const float2*>(w), Z, s, &ctx);
+    if (e == cudaSuccess) e = launch_inverse_modes(*p, Z, y, T, s, &ctx);
+    return cuda_status(e);
+}
+
+fno_status_t fno_forward_modes(fno_plan_t p, const float* x, void* X, void* ws, size_t ws_bytes,
+                               cudaStream_t s) {
+    if (!p) return FNO_ERR_INVALID_ARG;
+    fno_status_t st;
+    if ((st = check_device(p)) != FNO_OK) return st;
+    if ((st = check_ptr(x, true)) != FNO_OK) return st;
+    if ((st = check_ptr(X, true)) != FNO_OK) return st;
+    if ((st = check_ws(p, ws, ws_bytes)) != FNO_OK) return st;
+    if (overlaps(X, X_bytes(p), x, x_bytes(p))) return FNO_ERR_INVALID_ARG;
+    if (overlaps(ws, p->ws_bytes, x, x_bytes(p)) || overlaps(ws, p->ws_bytes, X, X_bytes(p)))
+        return FNO_ERR_INVALID_ARG;
+    float2* T = reinterpret_cast<float2*>(static_cast<char*>(ws) + p->off_T);
+    return cuda_status(launch_forward_modes(*p, x, static_cast<float2*>(X), T, s, nullptr));
+}
+
+fno_status_t fno_mix_modes(fno_plan_t p, const void* X, const void* w, void* Z, cudaStream_t s) {
+    if (!p) return FNO_ERR_INVALID_ARG;
+    fno_status_t st;
+    if ((st = check_device(p)) != FNO_OK) return st;
+    if ((st = check_ptr(X, true)) != FNO_OK) return st;
+    if ((st = check_ptr(w, true)) != FNO_OK) return st;
+    if ((st = check_ptr(Z, true)) != FNO_OK) return st;
+    if (overlaps(Z, Z_bytes(p), X, X_bytes(p)) || overlaps(Z, Z_bytes(p), w, w_bytes(p)))
+        return FNO_ERR_INVALID_ARG;
+    return cuda_status(launch_mix_modes(*p, static_cast<const float2*>(X),
+                                        static_cast<const float2*>(w), static_cast<float2*>(Z), s,
+                                        nullptr));
+}
+
+fno_status_t fno_inverse_modes(fno_plan_t p, const void* Z, float* y, void* ws, size_t ws_bytes,
+                               cudaStream_t s) {
+    if (!p) return FNO_ERR_INVALID_ARG;
+    fno_status_t st;
+    if ((st = check_device(p)) != FNO_OK) return st;
+    if ((st = check_ptr(Z, true)) != FNO_OK) return st;
+    if ((st = check_ptr(y, true)) != FNO_OK) return st;
+    if ((st = check_ws(p, ws, ws_bytes)) != FNO_OK) return st;
+    if (overlaps(y, y_bytes(p), Z, Z_bytes(p))) return FNO_ERR_INVALID_ARG;
+    if (overlaps(ws, p->ws_bytes, y, y_bytes(p)) || overlaps(ws, p->ws_bytes, Z, Z_bytes(p)))
+        return FNO_ERR_INVALID_ARG;
+    float2* T = reinterpret_cast<float2*>(static_cast<char*>(ws) + p->off_T);
+    return cuda_status(launch_inverse_modes(*p, static_cast<const float2*>(Z), y, T, s, nullptr));
+}
+
+fno_status_t fno_get_device_status(fno_plan_t p, cudaStream_t s) {
+    if (!p) return FNO_ERR_INVALID_ARG;
+    unsigned word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, p->err, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->err, 0, sizeof(unsigned), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return FNO_ERR_CUDA;
+    if (word & FNO_DEVERR_TIMEOUT) return FNO_ERR_TIMEOUT;
+    if (word) return FNO_ERR_DEVICE;
+    return FNO_OK;
+}
+
+}  // extern "C"
+
+// ---- one-shot API with a plan/workspace cache ------------------------------
+namespace {
+
+using PlanKey = std::tuple<int, int, int, int, int, int, int, int>;           // dev + shape
+using WsKey = std::tuple<int, int, int, int, int, int, int, int, uintptr_t>;  // + stream
+
+struct Cache {
+    std::mutex mu;
+    std::map<PlanKey, fno_plan_t> plans;
+    std::map<WsKey, std::pair<void*, size_t>> ws;
+};
+
+Cache& cache() {
+    static Cache* c = new Cache();  // intentionally leaked: no teardown-order issues at exit
+    return *c;
+}
+
+}  // namespace
+
+extern "C" fno_status_t fno_spectral_conv2d(const float* x, const void* w, float* y, int B,
+                                            int Cin, int Cout, int H, int W, int m1, int m2,
+                                            cudaStream_t s) {
+    fno_status_t st = validate_shape(B, Cin, Cout, H, W, m1, m2);
+    if (st != FNO_OK) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FNO_ERR_CUDA;
+    Cache& c = cache();
+    fno_plan_t plan = nullptr;
+    void* ws = nullptr;
+    size_t wsb = 0;
+    {
+        std::lock_guard<std::mutex> lock(c.mu);
+        PlanKey pk{dev, B, Cin, Cout, H, W, m1, m2};
+        auto it = c.plans.find(pk);
+        if (it == c.plans.end()) {
+            st = fno_plan_create(&plan, B, Cin, Cout, H, W, m1, m2, FNO_PREC_FP32);
+            if (st != FNO_OK) return st;
+            c.plans[pk] = plan;
+        } else {
+            plan = it->second;
+        }
+        WsKey wk{dev, B, Cin, Cout, H, W, m1, m2, reinterpret_cast<uintptr_t>(s)};
+        auto jt = c.ws.find(wk);
+        if (jt == c.ws.end()) {
+            wsb = plan->ws_bytes;
+            if (wsb && cudaMalloc(&ws, wsb) != cudaSuccess) return FNO_ERR_CUDA;
+            c.ws[wk] = {ws, wsb};
+        } else {
+            ws = jt->second.first;
+            wsb = jt->second.second;
+        }
+    }
+    return fno_plan_execute(plan, x, w, y, ws, wsb, s);
+}
+
+extern "C" fno_status_t fno_release_cache(void) {
+    Cache& c = cache();
+    std::lock_guard<std::mutex> lock(c.mu);
+    if (cudaDeviceSynchronize() != cudaSuccess) return FNO_ERR_CUDA;
+    for (auto& kv : c.ws)
+        if (kv.second.first) cudaFree(kv.second.first);
+    for (auto& kv : c.plans) fno_plan_destroy(kv.second);
+    c.ws.clear();
+    c.plans.clear();
+    return FNO_OK;
+}

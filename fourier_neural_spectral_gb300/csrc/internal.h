@@ -1,0 +1,65 @@
+// internal.h -- plan object and kernel launchers shared by the host files of
+// libfnospec.  Not part of the public ABI (that is include/fnospec.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "fnospec.h"
+
+// Bits of the device error word.
+enum : unsigned {
+    FNO_DEVERR_BOUNDS = 1u << 0,   // an index check in a kernel failed
+    FNO_DEVERR_TIMEOUT = 1u << 1,  // a bounded wait gave up
+};
+
+struct fno_kernel_desc {
+    char name[48];
+    size_t bytes;   // algorithmic bytes (compulsory reads + writes)
+    size_t flops;   // algorithmic flops
+};
+
+// Optional per-kernel event recording during one execute.
+struct fno_launch_ctx {
+    cudaEvent_t* events = nullptr;
+    int count = 0;
+    int next = 0;
+    cudaError_t mark(cudaStream_t s) {
+        if (!events || next >= count) return cudaSuccess;
+        return cudaEventRecord(events[next++], s);
+    }
+};
+
+constexpr int kMaxKernels = 8;
+
+struct fno_plan_s {
+    int B, Cin, Cout, H, W, m1, m2;
+    int nm;                 // retained modes per plane: 2*m1*m2
+    fno_precision_t prec;
+    int device;
+    float scale;            // 1/sqrt(H*W), rounded once from double
+    float2* tw_h;           // e^{+2 pi i j / H}, j in [0, H)
+    float2* tw_w;           // e^{+2 pi i j / W}, j in [0, W)
+    unsigned* err;          // device error word
+    // workspace layout (byte offsets, each 256-byte aligned)
+    size_t off_X, off_Z, off_T, ws_bytes;
+    int launches;           // kernel launches per execute
+    fno_kernel_desc kernels[kMaxKernels];
+    cudaEvent_t* events;    // armed per-kernel timing events (count = launches + 1)
+    int nevents;
+    char desc[256];
+};
+
+// One-time kernel attribute set-up (dynamic shared memory limits).
+cudaError_t stages_generic_init();
+cudaError_t mix_init();
+
+// Stage launchers (all asynchronous on stream s).
+// Each launcher calls ctx->mark(s) after every kernel it enqueues.
+cudaError_t launch_forward_modes(const fno_plan_s& p, const float* x, float2* X, float2* T,
+                                 cudaStream_t s, fno_launch_ctx* ctx);
+cudaError_t launch_mix_modes(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
+                             cudaStream_t s, fno_launch_ctx* ctx);
+cudaError_t launch_inverse_modes(const fno_plan_s& p, const float2* Z, float* y, float2* T,
+                                 cudaStream_t s, fno_launch_ctx* ctx);

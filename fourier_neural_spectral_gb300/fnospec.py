@@ -1,0 +1,242 @@
+"""Thin ctypes binding of libfnospec (include/fnospec.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  If the
+library is missing or fails to load, every entry point raises; there is no
+fallback computation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfnospec.so")
+
+FNO_OK = 0
+FNO_ERR_INVALID_ARG = 1
+FNO_ERR_UNSUPPORTED = 2
+FNO_ERR_CUDA = 3
+FNO_ERR_WORKSPACE = 4
+FNO_ERR_TIMEOUT = 5
+FNO_ERR_DEVICE = 6
+
+FNO_PREC_FP32 = 0
+FNO_PREC_TF32 = 1
+FNO_PREC_3XTF32 = 2
+PRECISIONS = {"fp32": FNO_PREC_FP32, "tf32": FNO_PREC_TF32, "3xtf32": FNO_PREC_3XTF32}
+
+# Every symbol include/fnospec.h declares.
+EXPORTS = (
+    "fno_status_string", "fno_plan_create", "fno_plan_workspace_size", "fno_plan_launch_count",
+    "fno_plan_describe", "fno_plan_kernel_info", "fno_plan_record_events", "fno_plan_execute", "fno_plan_destroy", "fno_spectral_conv2d",
+    "fno_release_cache", "fno_forward_modes", "fno_mix_modes", "fno_inverse_modes",
+    "fno_get_device_status",
+)
+
+
+class FnoError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libfnospec and declare the C signatures.  Raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libfnospec not built ({path} missing): run "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        st = ctypes.c_int
+        sig = {
+            "fno_status_string": (ctypes.c_char_p, [st]),
+            "fno_plan_create": (st, [ctypes.POINTER(vp), i, i, i, i, i, i, i, i]),
+            "fno_plan_workspace_size": (st, [vp, ctypes.POINTER(sz)]),
+            "fno_plan_launch_count": (st, [vp, ctypes.POINTER(i)]),
+            "fno_plan_describe": (st, [vp, ctypes.c_char_p, sz]),
+            "fno_plan_kernel_info": (st, [vp, i, ctypes.c_char_p, sz, ctypes.POINTER(sz),
+                                          ctypes.POINTER(sz)]),
+            "fno_plan_record_events": (st, [vp, ctypes.POINTER(vp), i]),
+            "fno_plan_execute": (st, [vp, vp, vp, vp, vp, sz, vp]),
+            "fno_plan_destroy": (st, [vp]),
+            "fno_spectral_conv2d": (st, [vp, vp, vp, i, i, i, i, i, i, i, vp]),
+            "fno_release_cache": (st, []),
+            "fno_forward_modes": (st, [vp, vp, vp, vp, sz, vp]),
+            "fno_mix_modes": (st, [vp, vp, vp, vp, vp]),
+            "fno_inverse_modes": (st, [vp, vp, vp, vp, sz, vp]),
+            "fno_get_device_status": (st, [vp, vp]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().fno_status_string(status).decode()
+    except Exception:
+        return f"status {status}"
+
+
+def _check(status: int, where: str):
+    if status != FNO_OK:
+        raise FnoError(status, where)
+
+
+def _ptr(t) -> int | None:
+    """Device address of a tensor, or an int/None passed through unchanged."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"expected a torch.Tensor or an address, got {type(t)}")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libfnospec must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _weight_ptr(w) -> int:
+    if isinstance(w, torch.Tensor) and w.dtype == torch.complex64:
+        return _ptr(w)
+    if isinstance(w, torch.Tensor) and w.dtype != torch.float32:
+        raise TypeError("w must be complex64 or float32 (re, im) pairs")
+    return _ptr(w)
+
+
+class Plan:
+    """fno_plan_t owner.  Holds its workspace as a torch tensor on the device."""
+
+    def __init__(self, B, Cin, Cout, H, W, m1, m2, precision="fp32", allocate_workspace=True):
+        lib = load_library()
+        prec = PRECISIONS[precision] if isinstance(precision, str) else int(precision)
+        h = ctypes.c_void_p()
+        _check(lib.fno_plan_create(ctypes.byref(h), B, Cin, Cout, H, W, m1, m2, prec),
+               "fno_plan_create")
+        self._h = h
+        self.shape = (B, Cin, Cout, H, W, m1, m2)
+        self.precision = precision
+        n = ctypes.c_size_t()
+        _check(lib.fno_plan_workspace_size(h, ctypes.byref(n)), "fno_plan_workspace_size")
+        self.workspace_bytes = int(n.value)
+        k = ctypes.c_int()
+        _check(lib.fno_plan_launch_count(h, ctypes.byref(k)), "fno_plan_launch_count")
+        self.launches = int(k.value)
+        buf = ctypes.create_string_buffer(256)
+        _check(lib.fno_plan_describe(h, buf, 256), "fno_plan_describe")
+        self.description = buf.value.decode()
+        self.kernels = []
+        for k in range(self.launches):
+            nm = ctypes.create_string_buffer(64)
+            nb, nf = ctypes.c_size_t(), ctypes.c_size_t()
+            _check(lib.fno_plan_kernel_info(h, k, nm, 64, ctypes.byref(nb), ctypes.byref(nf)),
+                   "fno_plan_kernel_info")
+            self.kernels.append({"name": nm.value.decode(), "bytes": int(nb.value),
+                                 "flops": int(nf.value)})
+        self._event_array = None
+        self.workspace = None
+        if allocate_workspace and self.workspace_bytes:
+            self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device="cuda")
+
+    @property
+    def handle(self):
+        return self._h
+
+    def _ws(self, workspace):
+        ws = self.workspace if workspace is None else workspace
+        nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+        return _ptr(ws), nbytes
+
+    def fno_plan_execute(self, x, w, y, workspace=None, stream=None):
+        wp, wn = self._ws(workspace)
+        _check(load_library().fno_plan_execute(self._h, _ptr(x), _weight_ptr(w), _ptr(y), wp, wn,
+                                               _stream(stream)), "fno_plan_execute")
+        return y
+
+    def fno_forward_modes(self, x, X, workspace=None, stream=None):
+        wp, wn = self._ws(workspace)
+        _check(load_library().fno_forward_modes(self._h, _ptr(x), _ptr(X), wp, wn,
+                                                _stream(stream)), "fno_forward_modes")
+        return X
+
+    def fno_mix_modes(self, X, w, Z, stream=None):
+        _check(load_library().fno_mix_modes(self._h, _ptr(X), _weight_ptr(w), _ptr(Z),
+                                            _stream(stream)), "fno_mix_modes")
+        return Z
+
+    def fno_inverse_modes(self, Z, y, workspace=None, stream=None):
+        wp, wn = self._ws(workspace)
+        _check(load_library().fno_inverse_modes(self._h, _ptr(Z), _ptr(y), wp, wn,
+                                                _stream(stream)), "fno_inverse_modes")
+        return y
+
+    def fno_plan_record_events(self, events):
+        """Arm per-kernel timing with a list of launches + 1 torch.cuda.Event
+        (created with enable_timing=True and already recorded once so that the
+        underlying CUDA event exists), or disarm with None."""
+        lib = load_library()
+        if events is None:
+            self._event_array = None
+            _check(lib.fno_plan_record_events(self._h, None, 0), "fno_plan_record_events")
+            return
+        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        self._event_array = arr  # keep alive while armed
+        _check(lib.fno_plan_record_events(self._h, arr, len(events)), "fno_plan_record_events")
+
+    def fno_get_device_status(self, stream=None) -> int:
+        return int(load_library().fno_get_device_status(self._h, _stream(stream)))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load_library().fno_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def fno_spectral_conv2d(x, w, y, B, Cin, Cout, H, W, m1, m2, stream=None):
+    """One-shot call with the exact C signature (fp32 path, cached plan)."""
+    _check(load_library().fno_spectral_conv2d(_ptr(x), _weight_ptr(w), _ptr(y), B, Cin, Cout, H,
+                                              W, m1, m2, _stream(stream)), "fno_spectral_conv2d")
+    return y
+
+
+def spectral_conv2d(x: torch.Tensor, w: torch.Tensor, m1: int, m2: int, out=None, stream=None):
+    """Convenience wrapper: shapes from the tensors, allocates y if needed."""
+    B, Cin, H, W = x.shape
+    Cout = w.shape[1]
+    if out is None:
+        out = torch.empty((B, Cout, H, W), dtype=torch.float32, device=x.device)
+    return fno_spectral_conv2d(x, w, out, B, Cin, Cout, H, W, m1, m2, stream)
+
+
+def fno_release_cache():
+    _check(load_library().fno_release_cache(), "fno_release_cache")

@@ -1,0 +1,160 @@
+/* fnospec.h -- C ABI of libfnospec, the FNO 2D spectral-convolution layer on one
+ * GPU (sm_103a).
+ *
+ * The layer (TurboFNO: FFT-GEMM-iFFT fused operator page, sections 1 and 2.2;
+ * orthonormal scaling per its section 3.1):
+ *
+ *   X = rfft2(x, norm="ortho")                    x : real [B][Cin][H][W]
+ *   Z[b,o,k1,k2] = sum_i X[b,i,k1,k2] * W[i,o,r,k2]   on the retained modes
+ *        k1 in R1 = {0..m1-1} U {H-m1..H-1},  k2 in R2 = {0..m2-1}
+ *   y = irfft2(Z, s=(H, W), norm="ortho")         y : real [B][Cout][H][W]
+ *
+ * with every bin outside R1 x R2 zero.  The complex-to-real row step keeps only
+ * the real part of the k2 = 0 bin (and of the k2 = W/2 bin when m2 = W/2 + 1),
+ * as the half-spectrum (W/2 + 1 wide) convention of the FFT operator-optimisation
+ * page (lpnh.cn/news/2688017, section 2.2) implies.
+ *
+ * Layouts (all dense, row-major, no padding, complex = interleaved re, im float):
+ *   x  float     [B][Cin][H][W]
+ *   w  complex64 [Cin][Cout][2*m1][m2]   retained row r: k1 = r for r < m1,
+ *                                        k1 = H - 2*m1 + r for r >= m1
+ *   y  float     [B][Cout][H][W]
+ *   X  complex64 [B][Cin][2*m1][m2]      (stage entry points only)
+ *   Z  complex64 [B][Cout][2*m1][m2]     (stage entry points only)
+ *
+ * Conventions shared by every entry point:
+ *   - Tensor pointers are DEVICE pointers (cudaMalloc / caching allocators /
+ *     managed memory) owned by the caller; the library never frees them.  Each
+ *     must be 16-byte aligned.  Unregistered host memory is rejected.
+ *   - Out-of-place only: outputs must not overlap inputs.
+ *   - Work is enqueued on the given stream and returns without synchronising
+ *     and without allocating (except the one-shot fno_spectral_conv2d, which
+ *     caches a plan and a workspace on its first call per shape and stream).
+ *   - Supported shapes: H and W powers of two in [2, 4096]; 1 <= m1, 2*m1 <= H;
+ *     1 <= m2 <= W/2 + 1; B, Cin, Cout >= 1; every tensor below 2^31 elements.
+ *   - Errors detected on the host are returned immediately and nothing is
+ *     enqueued.  Errors detected inside kernels set a word in device memory
+ *     that fno_get_device_status reads and clears.
+ */
+#ifndef FNOSPEC_H_
+#define FNOSPEC_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FNO_OK = 0,
+    FNO_ERR_INVALID_ARG = 1, /* null/misaligned/host pointer, bad size, aliasing */
+    FNO_ERR_UNSUPPORTED = 2, /* shape or precision outside what is built      */
+    FNO_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed     */
+    FNO_ERR_WORKSPACE = 4,   /* workspace smaller than fno_plan_workspace_size  */
+    FNO_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up              */
+    FNO_ERR_DEVICE = 6       /* a kernel flagged an internal error              */
+} fno_status_t;
+
+typedef enum {
+    /* fp32 storage and fp32 FMA for every stage. */
+    FNO_PREC_FP32 = 0,
+    /* Mode contraction on tcgen05 tensor cores with TF32 operands and fp32
+     * accumulation when Cin >= 32 and Cout >= 32 (fp32 FMA otherwise);
+     * transforms stay fp32.  Expected relative L2 error ~1e-3. */
+    FNO_PREC_TF32 = 1,
+    /* As FNO_PREC_TF32 but each operand is split into a TF32 high part and a
+     * TF32 residual and three products are accumulated (hi*hi + hi*lo + lo*hi),
+     * which recovers fp32-level accuracy on the tensor cores. */
+    FNO_PREC_3XTF32 = 2
+} fno_precision_t;
+
+typedef struct fno_plan_s* fno_plan_t;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* fno_status_string(fno_status_t status);
+
+/* Create a plan for one shape on the CURRENT device.  Host-side call: validates
+ * the shape, chooses the kernels, builds the twiddle tables (computed in double
+ * on the host, rounded once to float) and allocates them plus a device error
+ * word.  *plan is set to NULL on failure.
+ * Source for caching plans per shape: FFT operator-optimisation page, section
+ * 5.3 (reuse plans and workspace across calls; query the workspace size once). */
+fno_status_t fno_plan_create(fno_plan_t* plan, int B, int Cin, int Cout, int H, int W,
+                             int m1, int m2, fno_precision_t prec);
+
+/* Bytes of device workspace fno_plan_execute needs (may be 0). */
+fno_status_t fno_plan_workspace_size(fno_plan_t plan, size_t* bytes);
+
+/* Number of kernel launches one fno_plan_execute enqueues. */
+fno_status_t fno_plan_launch_count(fno_plan_t plan, int* launches);
+
+/* Copy a short description of the chosen kernels into buf (NUL-terminated). */
+fno_status_t fno_plan_describe(fno_plan_t plan, char* buf, size_t len);
+
+/* Describe kernel `index` (0-based, < fno_plan_launch_count) of one execute:
+ * its name (NUL-terminated, truncated to name_len), the algorithmic bytes it
+ * must move (compulsory reads + writes of its inputs and outputs, each once) and
+ * its algorithmic floating-point operations.  Any output pointer may be NULL. */
+fno_status_t fno_plan_kernel_info(fno_plan_t plan, int index, char* name, size_t name_len,
+                                  size_t* bytes, size_t* flops);
+
+/* Arm per-kernel timing for later executes: events[0] is recorded on the stream
+ * before the first kernel and events[k + 1] after kernel k, so count must be
+ * fno_plan_launch_count + 1.  The caller creates and owns the events.  Pass
+ * events = NULL (count 0) to disarm.  Not thread-safe against a concurrent
+ * execute of the same plan. */
+fno_status_t fno_plan_record_events(fno_plan_t plan, cudaEvent_t* events, int count);
+
+/* Run the whole layer y = irfft2(mix(rfft2(x), w)) on stream s.
+ * x: float [B][Cin][H][W]; w: complex64 [Cin][Cout][2*m1][m2];
+ * y: float [B][Cout][H][W]; workspace: device buffer of at least
+ * fno_plan_workspace_size bytes (NULL allowed when that size is 0), owned by the
+ * caller and not used concurrently by another call. */
+fno_status_t fno_plan_execute(fno_plan_t plan, const float* x, const void* w, float* y,
+                              void* workspace, size_t workspace_bytes, cudaStream_t s);
+
+/* Release the plan's tables and error word.  Safe on NULL.  The caller must make
+ * sure no work that uses the plan is still running. */
+fno_status_t fno_plan_destroy(fno_plan_t plan);
+
+/* One-shot form of fno_plan_execute with FNO_PREC_FP32.  Keeps an internal cache
+ * of plans keyed by (device, shape) and of workspaces keyed by (device, shape,
+ * stream); the first call for a key allocates (cudaMalloc), so make it before
+ * any stream capture.  Calls with the same key must not overlap on the GPU
+ * (they share the workspace). */
+fno_status_t fno_spectral_conv2d(const float* x, const void* w, float* y, int B, int Cin,
+                                 int Cout, int H, int W, int m1, int m2, cudaStream_t s);
+
+/* Free every cached plan and workspace of fno_spectral_conv2d (synchronises the
+ * device first). */
+fno_status_t fno_release_cache(void);
+
+/* Stage a1+a2 (forward row and column transforms, pruned to the retained modes,
+ * orthonormal scale applied): x float [B][Cin][H][W] -> X complex64
+ * [B][Cin][2*m1][m2].  Needs the plan's workspace. */
+fno_status_t fno_forward_modes(fno_plan_t plan, const float* x, void* X, void* workspace,
+                               size_t workspace_bytes, cudaStream_t s);
+
+/* Stage a3 (per-mode complex channel contraction): X complex64 [B][Cin][2*m1][m2],
+ * w complex64 [Cin][Cout][2*m1][m2] -> Z complex64 [B][Cout][2*m1][m2].
+ * Source: TurboFNO page, section 2.2 ((a+bi)(c+di) = (ac-bd) + (ad+bc)i per
+ * retained mode). */
+fno_status_t fno_mix_modes(fno_plan_t plan, const void* X, const void* w, void* Z,
+                           cudaStream_t s);
+
+/* Stage a4+a5 (zero-filled inverse column transform, complex-to-real row
+ * transform, orthonormal scale applied): Z complex64 [B][Cout][2*m1][m2] ->
+ * y float [B][Cout][H][W].  Needs the plan's workspace. */
+fno_status_t fno_inverse_modes(fno_plan_t plan, const void* Z, float* y, void* workspace,
+                               size_t workspace_bytes, cudaStream_t s);
+
+/* Synchronise stream s, read and clear the plan's device error word.  Returns
+ * FNO_OK, FNO_ERR_TIMEOUT or FNO_ERR_DEVICE (or FNO_ERR_CUDA if the copy fails). */
+fno_status_t fno_get_device_status(fno_plan_t plan, cudaStream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FNOSPEC_H_ */

@@ -1,0 +1,134 @@
+"""Edge shapes, invariants and error handling of the CUDA path."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+
+from gpu_helpers import (assert_fp32_close, f32pairs_to_cplx, rand_layer_inputs, run_layer,
+                         to_dev)
+
+pytestmark = pytest.mark.gpu
+
+EDGE_SHAPES = [
+    # B, Cin, Cout, H, W, m1, m2
+    (1, 1, 1, 2, 2, 1, 2),          # smallest grid, full modes incl. Nyquist
+    (3, 5, 7, 16, 64, 8, 33),       # 2*m1 = H and m2 = W/2 + 1 (Nyquist column kept)
+    (2, 3, 2, 64, 16, 1, 1),        # a single retained column / two rows
+    (2, 3, 4, 8, 128, 2, 65),       # wide, non-square, Nyquist
+    (1, 2, 3, 256, 4, 3, 3),        # tall, odd mode counts (ragged mode tile)
+    (17, 5, 17, 16, 16, 3, 5),      # B > 16 and Cout > 16: ragged batch / channel tiles
+    (1, 1, 1, 4096, 2, 1, 1),       # longest column transform
+    (1, 1, 2, 2, 4096, 1, 2049),    # longest row transform, every column kept
+    (2, 33, 31, 32, 32, 7, 9),      # channel counts off the tile sizes
+]
+
+
+@pytest.mark.parametrize("shape", EDGE_SHAPES)
+def test_edge_shapes_match_oracle(cuda_lib, shape):
+    B, Cin, Cout, H, W, m1, m2 = shape
+    rng = np.random.default_rng(sum(shape))
+    x, w = rand_layer_inputs(rng, B, Cin, Cout, H, W, m1, m2)
+    y, _ = run_layer(x, w, m1, m2)
+    ref = oracle.spectral_conv2d(x, f32pairs_to_cplx(w), m1, m2)
+    assert_fp32_close(y, ref, str(shape))
+
+
+@pytest.mark.parametrize("H,W", [(16, 16), (8, 64), (128, 32)])
+def test_identity_weights_full_modes_return_input(cuda_lib, H, W):
+    C, m1, m2 = 3, H // 2, W // 2 + 1
+    w = np.zeros((C, C, 2 * m1, m2, 2), np.float32)
+    for i in range(C):
+        w[i, i, :, :, 0] = 1.0
+    x = np.random.default_rng(1).standard_normal((2, C, H, W)).astype(np.float32)
+    y, _ = run_layer(x, w, m1, m2)
+    assert_fp32_close(y, x, "identity")
+
+
+def test_zero_input_gives_zero(cuda_lib):
+    x = np.zeros((2, 4, 32, 32), np.float32)
+    w = np.random.default_rng(2).random((4, 4, 8, 4, 2)).astype(np.float32)
+    y, _ = run_layer(x, w, 4, 4)
+    assert np.abs(y).max() == 0
+
+
+def test_linearity_and_shift_equivariance(cuda_lib):
+    rng = np.random.default_rng(3)
+    B, C, H, W, m1, m2 = 2, 8, 64, 32, 5, 6
+    x1, w = rand_layer_inputs(rng, B, C, C, H, W, m1, m2)
+    x2 = rng.standard_normal(x1.shape).astype(np.float32)
+    y1, plan = run_layer(x1, w, m1, m2)
+    y2, _ = run_layer(x2, w, m1, m2, plan=plan)
+    y12, _ = run_layer((x1 + 2 * x2).astype(np.float32), w, m1, m2, plan=plan)
+    assert_fp32_close(y12, y1.astype(np.float64) + 2 * y2, "linearity")
+    ys, _ = run_layer(np.roll(x1, (7, 3), axis=(2, 3)), w, m1, m2, plan=plan)
+    assert_fp32_close(ys, np.roll(y1, (7, 3), axis=(2, 3)), "shift")
+
+
+# ------------------------------------------------------------ error paths ---
+
+@pytest.fixture()
+def small_plan(cuda_lib):
+    from fourier_neural_spectral_gb300 import fnospec
+    return fnospec.Plan(2, 4, 4, 16, 16, 4, 4)
+
+
+def _tensors(plan):
+    import torch
+    x = torch.randn(2, 4, 16, 16, device="cuda")
+    w = torch.rand(4, 4, 8, 4, 2, device="cuda")
+    y = torch.empty(2, 4, 16, 16, device="cuda")
+    return x, w, y
+
+
+def test_misaligned_pointer_rejected(small_plan):
+    from fourier_neural_spectral_gb300 import fnospec
+    x, w, y = _tensors(small_plan)
+    with pytest.raises(fnospec.FnoError) as e:
+        small_plan.fno_plan_execute(x.data_ptr() + 4, w, y)
+    assert e.value.status == fnospec.FNO_ERR_INVALID_ARG
+
+
+def test_host_pointer_rejected(small_plan):
+    from fourier_neural_spectral_gb300 import fnospec
+    x, w, y = _tensors(small_plan)
+    host = np.zeros(2 * 4 * 16 * 16 + 64, np.float32)
+    addr = (host.ctypes.data + 15) // 16 * 16
+    with pytest.raises(fnospec.FnoError) as e:
+        small_plan.fno_plan_execute(addr, w, y)
+    assert e.value.status == fnospec.FNO_ERR_INVALID_ARG
+
+
+def test_aliasing_rejected(small_plan):
+    from fourier_neural_spectral_gb300 import fnospec
+    x, w, y = _tensors(small_plan)
+    with pytest.raises(fnospec.FnoError) as e:
+        small_plan.fno_plan_execute(x, w, x)
+    assert e.value.status == fnospec.FNO_ERR_INVALID_ARG
+
+
+def test_small_workspace_rejected(small_plan):
+    import torch
+    from fourier_neural_spectral_gb300 import fnospec
+    x, w, y = _tensors(small_plan)
+    ws = torch.empty(small_plan.workspace_bytes - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fnospec.FnoError) as e:
+        small_plan.fno_plan_execute(x, w, y, workspace=ws)
+    assert e.value.status == fnospec.FNO_ERR_WORKSPACE
+
+
+def test_null_pointer_rejected(small_plan):
+    from fourier_neural_spectral_gb300 import fnospec
+    x, w, y = _tensors(small_plan)
+    with pytest.raises(fnospec.FnoError) as e:
+        small_plan.fno_plan_execute(x, None, y)
+    assert e.value.status == fnospec.FNO_ERR_INVALID_ARG
+
+
+def test_device_status_clean_after_runs(small_plan):
+    from fourier_neural_spectral_gb300 import fnospec
+    x, w, y = _tensors(small_plan)
+    for _ in range(3):
+        small_plan.fno_plan_execute(x, w, y)
+    assert small_plan.fno_get_device_status() == fnospec.FNO_OK
