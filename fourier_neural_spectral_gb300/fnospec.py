@@ -34,7 +34,7 @@ EXPORTS = (
     "fno_status_string", "fno_plan_create", "fno_plan_workspace_size", "fno_plan_launch_count",
     "fno_plan_describe", "fno_plan_kernel_info", "fno_plan_record_events", "fno_plan_execute", "fno_plan_destroy", "fno_spectral_conv2d",
     "fno_release_cache", "fno_forward_modes", "fno_mix_modes", "fno_inverse_modes",
-    "fno_get_device_status",
+    "fno_get_device_status", "fno_spectral_conv2d_noalloc",
 )
 
 
@@ -78,6 +78,7 @@ def load_library(path: str = LIB_PATH):
             "fno_mix_modes": (st, [vp, vp, vp, vp, vp]),
             "fno_inverse_modes": (st, [vp, vp, vp, vp, sz, vp]),
             "fno_get_device_status": (st, [vp, vp]),
+            "fno_spectral_conv2d_noalloc": (st, [vp, vp, vp, i, i, i, i, i, i, i, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -226,6 +227,15 @@ def fno_spectral_conv2d(x, w, y, B, Cin, Cout, H, W, m1, m2, stream=None):
     """One-shot call with the exact C signature (fp32 path, cached plan)."""
     _check(load_library().fno_spectral_conv2d(_ptr(x), _weight_ptr(w), _ptr(y), B, Cin, Cout, H,
                                               W, m1, m2, _stream(stream)), "fno_spectral_conv2d")
+    return y
+
+
+def fno_spectral_conv2d_noalloc(x, w, y, B, Cin, Cout, H, W, m1, m2, stream=None):
+    """The layer without any device allocation (static scratch inside the
+    library, small shapes only); see include/fnospec.h."""
+    _check(load_library().fno_spectral_conv2d_noalloc(_ptr(x), _weight_ptr(w), _ptr(y), B, Cin,
+                                                      Cout, H, W, m1, m2, _stream(stream)),
+           "fno_spectral_conv2d_noalloc")
     return y
 
 

@@ -149,6 +149,25 @@ fno_status_t fno_mix_modes(fno_plan_t plan, const void* X, const void* w, void* 
 fno_status_t fno_inverse_modes(fno_plan_t plan, const void* Z, float* y, void* workspace,
                                size_t workspace_bytes, cudaStream_t s);
 
+/* The whole layer (same arguments and result as fno_spectral_conv2d, fp32
+ * path) for callers that cannot allocate device memory: this entry point calls
+ * no cudaMalloc, cudaFree or other allocating routine.  The pages have no
+ * counterpart; it exists for hosts that own every allocation themselves.
+ * Its scratch (twiddle tables, error word, the spectra X and Z, the row/column
+ * intermediate) lives in one static device array of 16 MiB that every GPU
+ * loading the library holds until exit; shapes whose scratch does not fit
+ * (2*m1*m2*8*B*(Cin+Cout) + 8*B*max(Cin,Cout)*H*m2 + 8*(H+W) bytes, plus
+ * alignment) return FNO_ERR_UNSUPPORTED before anything is enqueued.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) while that device is current; make that first call
+ * before any stream capture.  All calls share the array and each call
+ * re-initialises what it reads, so calls that overlap on the GPU (different
+ * streams, or several host threads) race and must be serialised by the
+ * caller. */
+fno_status_t fno_spectral_conv2d_noalloc(const float* x, const void* w, float* y, int B,
+                                         int Cin, int Cout, int H, int W, int m1, int m2,
+                                         cudaStream_t s);
+
 /* Synchronise stream s, read and clear the plan's device error word.  Returns
  * FNO_OK, FNO_ERR_TIMEOUT or FNO_ERR_DEVICE (or FNO_ERR_CUDA if the copy fails). */
 fno_status_t fno_get_device_status(fno_plan_t plan, cudaStream_t s);
