@@ -107,6 +107,30 @@ void describe_generic(fno_plan_s* p) {
     p->launches = 5;
 }
 
+// Kernel list of the fused path (stages_fused.cu + mix_fma.cu).
+void describe_fused(fno_plan_s* p) {
+    const size_t Pi = (size_t)p->B * p->Cin, Po = (size_t)p->B * p->Cout;
+    int k = 0;
+    if (p->P > 1) set_kernel(p, k++, "zero_X", X_bytes(p), 0);
+    const double fl_f = Pi * (fft_flops(p->W) * p->H / 2 + fft_flops(p->R) * p->m2 * p->P);
+    const double fl_i = Po * (fft_flops(p->W) * p->H / 2 + fft_flops(p->R) * p->m2 * p->P);
+    set_kernel(p, k++, "fwd_fused", x_bytes(p) + X_bytes(p), (size_t)fl_f);
+    set_kernel(p, k++, "mix_fma", X_bytes(p) + w_bytes(p) + Z_bytes(p),
+               8ull * p->B * p->Cin * p->Cout * p->nm);
+    set_kernel(p, k++, "inv_fused", Z_bytes(p) + y_bytes(p), (size_t)fl_i);
+    p->launches = k;
+}
+
+cudaError_t run_forward(const fno_plan_s& p, const float* x, float2* X, float2* T, cudaStream_t s,
+                        fno_launch_ctx* ctx) {
+    return p.path == 1 ? launch_forward_fused(p, x, X, s, ctx) : launch_forward_modes(p, x, X, T, s, ctx);
+}
+
+cudaError_t run_inverse(const fno_plan_s& p, const float2* Z, float* y, float2* T, cudaStream_t s,
+                        fno_launch_ctx* ctx) {
+    return p.path == 1 ? launch_inverse_fused(p, Z, y, s, ctx) : launch_inverse_modes(p, Z, y, T, s, ctx);
+}
+
 fno_status_t cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return FNO_OK;
     return FNO_ERR_CUDA;
@@ -144,6 +168,7 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
 
     std::call_once(g_init_once, [] {
         g_init_err = stages_generic_init();
+        if (g_init_err == cudaSuccess) g_init_err = stages_fused_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_init();
     });
     if (g_init_err != cudaSuccess) return FNO_ERR_CUDA;
@@ -156,17 +181,31 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     p->scale = (float)(1.0 / std::sqrt((double)H * (double)W));
     if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return FNO_ERR_CUDA; }
 
-    // workspace: X | Z | T
+    int R = 0;
+    p->path = fused_supported(W, H, m1, m2, &R) ? 1 : 0;
+    p->R = p->path == 1 ? R : H;
+    p->P = H / p->R;
+
+    // workspace: X | Z | T (T only on the shape-generic path)
     size_t off = 0;
     p->off_X = off; off = align_up(off + X_bytes(p), 256);
     p->off_Z = off; off = align_up(off + Z_bytes(p), 256);
     p->off_T = off;
-    const size_t planes = (size_t)B * (Cin > Cout ? Cin : Cout);
-    off = align_up(off + 8ull * planes * H * m2, 256);
+    if (p->path == 0) {
+        const size_t planes = (size_t)B * (Cin > Cout ? Cin : Cout);
+        off = align_up(off + 8ull * planes * H * m2, 256);
+    }
     p->ws_bytes = off;
-    describe_generic(p);
-    std::snprintf(p->desc, sizeof(p->desc),
-                  "generic: rows-fft(W=%d)|cols-fft(H=%d)|mix-fma|icols-fft|irows-fft, fp32", W, H);
+    if (p->path == 1) {
+        describe_fused(p);
+        std::snprintf(p->desc, sizeof(p->desc),
+                      "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|mix-fma|inv-cols+rows, fp32", W, p->R,
+                      p->P);
+    } else {
+        describe_generic(p);
+        std::snprintf(p->desc, sizeof(p->desc),
+                      "generic: rows-fft(W=%d)|cols-fft(H=%d)|mix-fma|icols-fft|irows-fft, fp32", W, H);
+    }
 
     std::vector<float2> th = twiddles(H), tw = twiddles(W);
     cudaError_t e = cudaMalloc(&p->tw_h, sizeof(float2) * H);
@@ -255,9 +294,9 @@ fno_status_t fno_plan_execute(fno_plan_t p, const float* x, const void* w, float
     ctx.events = p->events;
     ctx.count = p->nevents;
     cudaError_t e = ctx.mark(s);
-    if (e == cudaSuccess) e = launch_forward_modes(*p, x, X, T, s, &ctx);
+    if (e == cudaSuccess) e = run_forward(*p, x, X, T, s, &ctx);
     if (e == cudaSuccess) e = launch_mix_modes(*p, X, static_cast<const float2*>(w), Z, s, &ctx);
-    if (e == cudaSuccess) e = launch_inverse_modes(*p, Z, y, T, s, &ctx);
+    if (e == cudaSuccess) e = run_inverse(*p, Z, y, T, s, &ctx);
     return cuda_status(e);
 }
 
@@ -273,7 +312,7 @@ fno_status_t fno_forward_modes(fno_plan_t p, const float* x, void* X, void* ws, 
     if (overlaps(ws, p->ws_bytes, x, x_bytes(p)) || overlaps(ws, p->ws_bytes, X, X_bytes(p)))
         return FNO_ERR_INVALID_ARG;
     float2* T = reinterpret_cast<float2*>(static_cast<char*>(ws) + p->off_T);
-    return cuda_status(launch_forward_modes(*p, x, static_cast<float2*>(X), T, s, nullptr));
+    return cuda_status(run_forward(*p, x, static_cast<float2*>(X), T, s, nullptr));
 }
 
 fno_status_t fno_mix_modes(fno_plan_t p, const void* X, const void* w, void* Z, cudaStream_t s) {
@@ -302,7 +341,7 @@ fno_status_t fno_inverse_modes(fno_plan_t p, const void* Z, float* y, void* ws, 
     if (overlaps(ws, p->ws_bytes, y, y_bytes(p)) || overlaps(ws, p->ws_bytes, Z, Z_bytes(p)))
         return FNO_ERR_INVALID_ARG;
     float2* T = reinterpret_cast<float2*>(static_cast<char*>(ws) + p->off_T);
-    return cuda_status(launch_inverse_modes(*p, static_cast<const float2*>(Z), y, T, s, nullptr));
+    return cuda_status(run_inverse(*p, static_cast<const float2*>(Z), y, T, s, nullptr));
 }
 
 fno_status_t fno_get_device_status(fno_plan_t p, cudaStream_t s) {

@@ -44,6 +44,8 @@ struct fno_plan_s {
     unsigned* err;          // device error word
     // workspace layout (byte offsets, each 256-byte aligned)
     size_t off_X, off_Z, off_T, ws_bytes;
+    int path;               // 0: shape-generic kernels, 1: fused transform kernels
+    int R, P;               // fused path: column length per CTA and H / R
     int launches;           // kernel launches per execute
     fno_kernel_desc kernels[kMaxKernels];
     cudaEvent_t* events;    // armed per-kernel timing events (count = launches + 1)
@@ -54,6 +56,15 @@ struct fno_plan_s {
 // One-time kernel attribute set-up (dynamic shared memory limits).
 cudaError_t stages_generic_init();
 cudaError_t mix_init();
+
+// Fused transform kernels (stages_fused.cu).
+cudaError_t stages_fused_init();
+bool fused_supported(int W, int H, int m1, int m2, int* R_out);
+size_t fused_smem_bytes_any(int W, int R, int m2);
+cudaError_t launch_forward_fused(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s,
+                                 fno_launch_ctx* ctx);
+cudaError_t launch_inverse_fused(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s,
+                                 fno_launch_ctx* ctx);
 
 // Stage launchers (all asynchronous on stream s).
 // Each launcher calls ctx->mark(s) after every kernel it enqueues.

@@ -22,6 +22,13 @@ EDGE_SHAPES = [
     (1, 1, 1, 4096, 2, 1, 1),       # longest column transform
     (1, 1, 2, 2, 4096, 1, 2049),    # longest row transform, every column kept
     (2, 33, 31, 32, 32, 7, 9),      # channel counts off the tile sizes
+    # fused transform path: row groups h = p + P*q with P > 1, Nyquist, non-square
+    (2, 3, 4, 512, 64, 16, 9),      # R = 32, P = 16
+    (1, 2, 2, 1024, 128, 64, 65),   # R = 128, P = 8, Nyquist column kept
+    (2, 4, 4, 64, 256, 32, 129),    # 2*m1 = H, m2 = W/2 + 1
+    (2, 3, 5, 256, 32, 128, 17),    # every row retained, narrow rows
+    (3, 2, 3, 128, 64, 5, 7),       # odd mode counts inside the fused path
+    (2, 4, 6, 2048, 32, 64, 16),    # tall grid: R = 128, P = 16
 ]
 
 
