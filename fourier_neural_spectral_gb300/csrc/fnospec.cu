@@ -100,7 +100,7 @@ void describe_generic(fno_plan_s* p) {
     const size_t Ti = 8ull * Pi * p->H * p->m2, To = 8ull * Po * p->H * p->m2;
     set_kernel(p, 0, "fwd_rows", x_bytes(p) + Ti, (size_t)(fft_flops(p->W) * Pi * p->H / 2));
     set_kernel(p, 1, "fwd_cols", Ti + X_bytes(p), (size_t)(fft_flops(p->H) * Pi * p->m2));
-    set_kernel(p, 2, "mix_fma", X_bytes(p) + w_bytes(p) + Z_bytes(p),
+    set_kernel(p, 2, p->mix_path == 1 ? "mix_tma" : "mix_fma", X_bytes(p) + w_bytes(p) + Z_bytes(p),
                8ull * p->B * p->Cin * p->Cout * p->nm);
     set_kernel(p, 3, "inv_cols", Z_bytes(p) + To, (size_t)(fft_flops(p->H) * Po * p->m2));
     set_kernel(p, 4, "inv_rows", To + y_bytes(p), (size_t)(fft_flops(p->W) * Po * p->H / 2));
@@ -115,7 +115,7 @@ void describe_fused(fno_plan_s* p) {
     const double fl_f = Pi * (fft_flops(p->W) * p->H / 2 + fft_flops(p->R) * p->m2 * p->P);
     const double fl_i = Po * (fft_flops(p->W) * p->H / 2 + fft_flops(p->R) * p->m2 * p->P);
     set_kernel(p, k++, "fwd_fused", x_bytes(p) + X_bytes(p), (size_t)fl_f);
-    set_kernel(p, k++, "mix_fma", X_bytes(p) + w_bytes(p) + Z_bytes(p),
+    set_kernel(p, k++, p->mix_path == 1 ? "mix_tma" : "mix_fma", X_bytes(p) + w_bytes(p) + Z_bytes(p),
                8ull * p->B * p->Cin * p->Cout * p->nm);
     set_kernel(p, k++, "inv_fused", Z_bytes(p) + y_bytes(p), (size_t)fl_i);
     p->launches = k;
@@ -129,6 +129,11 @@ cudaError_t run_forward(const fno_plan_s& p, const float* x, float2* X, float2* 
 cudaError_t run_inverse(const fno_plan_s& p, const float2* Z, float* y, float2* T, cudaStream_t s,
                         fno_launch_ctx* ctx) {
     return p.path == 1 ? launch_inverse_fused(p, Z, y, s, ctx) : launch_inverse_modes(p, Z, y, T, s, ctx);
+}
+
+cudaError_t run_mix(const fno_plan_s& p, const float2* X, const float2* w, float2* Z, cudaStream_t s,
+                    fno_launch_ctx* ctx) {
+    return p.mix_path == 1 ? launch_mix_tma(p, X, w, Z, s, ctx) : launch_mix_modes(p, X, w, Z, s, ctx);
 }
 
 fno_status_t cuda_status(cudaError_t e) {
@@ -170,6 +175,7 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
         g_init_err = stages_generic_init();
         if (g_init_err == cudaSuccess) g_init_err = stages_fused_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_init();
+        if (g_init_err == cudaSuccess) g_init_err = mix_tma_init();
     });
     if (g_init_err != cudaSuccess) return FNO_ERR_CUDA;
 
@@ -185,6 +191,7 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     p->path = fused_supported(W, H, m1, m2, &R) ? 1 : 0;
     p->R = p->path == 1 ? R : H;
     p->P = H / p->R;
+    p->mix_path = mix_tma_supported(B, Cin, Cout, p->nm) ? 1 : 0;
 
     // workspace: X | Z | T (T only on the shape-generic path)
     size_t off = 0;
@@ -199,12 +206,13 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     if (p->path == 1) {
         describe_fused(p);
         std::snprintf(p->desc, sizeof(p->desc),
-                      "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|mix-fma|inv-cols+rows, fp32", W, p->R,
-                      p->P);
+                      "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|%s|inv-cols+rows, fp32", W, p->R,
+                      p->P, p->mix_path == 1 ? "mix-tma" : "mix-fma");
     } else {
         describe_generic(p);
         std::snprintf(p->desc, sizeof(p->desc),
-                      "generic: rows-fft(W=%d)|cols-fft(H=%d)|mix-fma|icols-fft|irows-fft, fp32", W, H);
+                      "generic: rows-fft(W=%d)|cols-fft(H=%d)|%s|icols-fft|irows-fft, fp32", W, H,
+                      p->mix_path == 1 ? "mix-tma" : "mix-fma");
     }
 
     std::vector<float2> th = twiddles(H), tw = twiddles(W);
@@ -295,7 +303,7 @@ fno_status_t fno_plan_execute(fno_plan_t p, const float* x, const void* w, float
     ctx.count = p->nevents;
     cudaError_t e = ctx.mark(s);
     if (e == cudaSuccess) e = run_forward(*p, x, X, T, s, &ctx);
-    if (e == cudaSuccess) e = launch_mix_modes(*p, X, static_cast<const float2*>(w), Z, s, &ctx);
+    if (e == cudaSuccess) e = run_mix(*p, X, static_cast<const float2*>(w), Z, s, &ctx);
     if (e == cudaSuccess) e = run_inverse(*p, Z, y, T, s, &ctx);
     return cuda_status(e);
 }
@@ -324,9 +332,8 @@ fno_status_t fno_mix_modes(fno_plan_t p, const void* X, const void* w, void* Z, 
     if ((st = check_ptr(Z, true)) != FNO_OK) return st;
     if (overlaps(Z, Z_bytes(p), X, X_bytes(p)) || overlaps(Z, Z_bytes(p), w, w_bytes(p)))
         return FNO_ERR_INVALID_ARG;
-    return cuda_status(launch_mix_modes(*p, static_cast<const float2*>(X),
-                                        static_cast<const float2*>(w), static_cast<float2*>(Z), s,
-                                        nullptr));
+    return cuda_status(run_mix(*p, static_cast<const float2*>(X), static_cast<const float2*>(w),
+                               static_cast<float2*>(Z), s, nullptr));
 }
 
 fno_status_t fno_inverse_modes(fno_plan_t p, const void* Z, float* y, void* ws, size_t ws_bytes,

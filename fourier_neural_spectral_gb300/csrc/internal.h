@@ -45,6 +45,7 @@ struct fno_plan_s {
     // workspace layout (byte offsets, each 256-byte aligned)
     size_t off_X, off_Z, off_T, ws_bytes;
     int path;               // 0: shape-generic kernels, 1: fused transform kernels
+    int mix_path;           // 0: mix_fma (shared-memory tiles), 1: mix_tma (TMA-fed)
     int R, P;               // fused path: column length per CTA and H / R
     int launches;           // kernel launches per execute
     fno_kernel_desc kernels[kMaxKernels];
@@ -65,6 +66,12 @@ cudaError_t launch_forward_fused(const fno_plan_s& p, const float* x, float2* X,
                                  fno_launch_ctx* ctx);
 cudaError_t launch_inverse_fused(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s,
                                  fno_launch_ctx* ctx);
+
+// TMA-fed fp32 contraction (mix_tma.cu).
+cudaError_t mix_tma_init();
+bool mix_tma_supported(int B, int Cin, int Cout, int nm);
+cudaError_t launch_mix_tma(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
+                           cudaStream_t s, fno_launch_ctx* ctx);
 
 // Stage launchers (all asynchronous on stream s).
 // Each launcher calls ctx->mark(s) after every kernel it enqueues.

@@ -29,6 +29,10 @@ EDGE_SHAPES = [
     (2, 3, 5, 256, 32, 128, 17),    # every row retained, narrow rows
     (3, 2, 3, 128, 64, 5, 7),       # odd mode counts inside the fused path
     (2, 4, 6, 2048, 32, 64, 16),    # tall grid: R = 128, P = 16
+    # TMA-fed contraction: ragged boxes
+    (3, 33, 40, 32, 32, 3, 5),      # B < batch tile, Cin % IC != 0, Cout % 32 != 0, NM % 4 == 2
+    (5, 16, 96, 64, 32, 4, 4),      # B = 5 -> batch tile 8 split over two warp groups
+    (20, 32, 32, 32, 32, 2, 3),     # B > 16: two batch tiles
 ]
 
 
