@@ -120,4 +120,18 @@ __device__ __forceinline__ int row_of_residue(int f, int R, int H, int m1, int* 
     return -1;
 }
 
+// Packed spectrum bin k of U = S_a + i S_b (the Hermitian extensions of the kept
+// bins of rows a and b, imaginary parts of k = 0 and k = W/2 dropped), for
+// k <= W/2, and the value of its mirror bin W - k.
+__device__ __forceinline__ void packed_bin(float2 a, float2 b, bool self_mirror, float2* uk,
+                                           float2* um) {
+    if (self_mirror) {
+        *uk = make_float2(a.x, b.x);
+        *um = *uk;
+    } else {
+        *uk = make_float2(a.x - b.y, a.y + b.x);  // Va + i Vb
+        *um = make_float2(a.x + b.y, b.x - a.y);  // conj Va + i conj Vb
+    }
+}
+
 }  // namespace fno

@@ -174,6 +174,7 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     std::call_once(g_init_once, [] {
         g_init_err = stages_generic_init();
         if (g_init_err == cudaSuccess) g_init_err = stages_fused_init();
+        if (g_init_err == cudaSuccess) g_init_err = stages_big_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_tma_init();
     });

@@ -1,0 +1,137 @@
+// fused_columns.cuh -- the column halves of the fused transform kernels,
+// shared by the kernels for short rows (stages_fused.cu) and long rows
+// (stages_big.cu).  256 threads; R is the column length (32..256).
+//
+// Forward: every kept column k2 of Y[q][k2] (q in [0, R)) is transformed with an
+// R-point DFT split as R = 16 * (R/16): a 16-point register DFT over the rows
+// q = n1 + (R/16)*n2, twiddle e^{-2 pi i n1 kk / R}, shared-memory transpose,
+// then (R/16)-point DFTs.  Output residue f holds the retained frequency k1
+// with k1 = f mod R (R >= 2*m1); it is scaled by 1/sqrt(HW) and stored to X
+// (P = 1) or multiplied by e^{-2 pi i k1 p / H} and added to X (P > 1).
+// Inverse: the mirror (decimation in time) with inputs read from Z.
+#pragma once
+
+#include "fft_reg.cuh"
+
+namespace fno {
+
+constexpr int kColThreads = 256;
+
+template <int R>
+struct ColCfg {
+    static constexpr int Bq = R / 16;
+    static constexpr int CP = kColThreads / Bq;  // columns per pass
+    static constexpr int Scr = R + 17;           // per-column scratch (== 1 mod 16)
+    static constexpr int Scratch = CP * Scr;
+};
+
+template <int R>
+__device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, int ys,
+                                                float2* __restrict__ X, size_t xbase, int H,
+                                                int m1, int m2, int P, int p, float scale,
+                                                const float2* __restrict__ tw_h) {
+    constexpr int Bq = ColCfg<R>::Bq;
+    constexpr int J = 16 / Bq;
+    constexpr int CP = ColCfg<R>::CP;
+    const int cs = threadIdx.x % CP;   // column within the pass
+    const int n1 = threadIdx.x / CP;   // position within the column transform
+    float2* S = scr + cs * ColCfg<R>::Scr;  // S[kk][n1] with row stride Bq
+    for (int c0 = 0; c0 < m2; c0 += CP) {
+        const int col = c0 + cs;
+        const bool active = col < m2;
+        if (active) {
+            float2 v[16];
+#pragma unroll
+            for (int n2 = 0; n2 < 16; ++n2) v[n2] = Y[(n1 + Bq * n2) * ys + col];
+            dft<16, -1>(v);
+#pragma unroll
+            for (int kk = 1; kk < 16; ++kk) v[kk] = cmul(v[kk], root<-1>(tw_h, n1 * kk * P, H));
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) S[kk * Bq + n1] = v[kk];
+        }
+        __syncthreads();
+        if (active) {
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int kk = n1 + Bq * j;
+                float2 u[Bq];
+#pragma unroll
+                for (int t = 0; t < Bq; ++t) u[t] = S[kk * Bq + t];
+                dft<Bq, -1>(u);
+#pragma unroll
+                for (int k1 = 0; k1 < Bq; ++k1) {
+                    int kf;
+                    const int r = row_of_residue(16 * k1 + kk, R, H, m1, &kf);
+                    if (r < 0) continue;
+                    float2 val = cscale(u[k1], scale);
+                    float2* dst = X + xbase + (size_t)r * m2 + col;
+                    if (P == 1) {
+                        *dst = val;
+                    } else {
+                        val = cmul(val, root<-1>(tw_h, kf * p, H));
+                        atomicAdd(&dst->x, val.x);
+                        atomicAdd(&dst->y, val.y);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int R>
+__device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys,
+                                                const float2* __restrict__ Zp, int H, int m1,
+                                                int m2, int P, int p,
+                                                const float2* __restrict__ tw_h) {
+    constexpr int Bq = ColCfg<R>::Bq;
+    constexpr int J = 16 / Bq;
+    constexpr int CP = ColCfg<R>::CP;
+    const int cs = threadIdx.x % CP;
+    const int t = threadIdx.x / CP;
+    float2* S = scr + cs * ColCfg<R>::Scr;  // S[n1][kk] with row stride 16
+    for (int c0 = 0; c0 < m2; c0 += CP) {
+        const int col = c0 + cs;
+        const bool active = col < m2;
+        if (active) {
+            // pass 1 (transposed): for kk = t + Bq*j, inverse Bq-point DFT over
+            // k1 of U[16*k1 + kk], then times e^{+2 pi i n1 kk / R}
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int kk = t + Bq * j;
+                float2 u[Bq];
+#pragma unroll
+                for (int k1 = 0; k1 < Bq; ++k1) {
+                    int kf;
+                    const int r = row_of_residue(16 * k1 + kk, R, H, m1, &kf);
+                    float2 val = make_float2(0.f, 0.f);
+                    if (r >= 0) {
+                        val = __ldg(&Zp[(size_t)r * m2 + col]);
+                        if (P > 1) val = cmul(val, root<1>(tw_h, kf * p, H));
+                    }
+                    u[k1] = val;
+                }
+                dft<Bq, 1>(u);
+#pragma unroll
+                for (int n1 = 0; n1 < Bq; ++n1) {
+                    const float2 w = n1 == 0 ? u[n1] : cmul(u[n1], root<1>(tw_h, n1 * kk * P, H));
+                    S[n1 * 16 + kk] = w;
+                }
+            }
+        }
+        __syncthreads();
+        if (active) {
+            // pass 2: thread n1 = t, inverse 16-point DFT over kk
+            const int n1 = t;
+            float2 v[16];
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) v[kk] = S[n1 * 16 + kk];
+            dft<16, 1>(v);
+#pragma unroll
+            for (int n2 = 0; n2 < 16; ++n2) V[(n1 + Bq * n2) * ys + col] = v[n2];
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace fno

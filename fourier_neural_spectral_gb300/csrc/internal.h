@@ -66,6 +66,11 @@ cudaError_t launch_forward_fused(const fno_plan_s& p, const float* x, float2* X,
                                  fno_launch_ctx* ctx);
 cudaError_t launch_inverse_fused(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s,
                                  fno_launch_ctx* ctx);
+// Long-row variants (stages_big.cu), W in {512, 1024, 2048, 4096}, m2 <= 64.
+cudaError_t stages_big_init();
+size_t big_smem_bytes_any(int W, int R, int m2);
+cudaError_t launch_forward_big(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s);
+cudaError_t launch_inverse_big(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s);
 
 // TMA-fed fp32 contraction (mix_tma.cu).
 cudaError_t mix_tma_init();

@@ -25,7 +25,7 @@ namespace {
 constexpr int kStages = 6;
 
 struct MixTmaCfg {
-    int OC, IC, BT, BTT, NBH;
+    int OC, IC, BT, BTT, NBH, OT;
     size_t w_off, x_off, stage_bytes, smem;
 };
 
@@ -39,7 +39,8 @@ MixTmaCfg mix_tma_cfg(int B, int Cin, int Cout) {
     c.BT = bt;
     c.BTT = std::min(bt, 8);
     c.NBH = bt / c.BTT;
-    if (c.OC * c.NBH > 256) c.OC = 256 / c.NBH;
+    c.OT = c.OC >= 64 ? 2 : 1;  // output channels per thread
+    if (c.OC / c.OT * c.NBH > 256) c.OC = 256 * c.OT / c.NBH;
     c.IC = std::max(1, std::min(Cin, 8192 / (32 * c.OC)));
     // one stage: w box (8 floats, OC, IC) then X box (8 floats, IC, BT)
     c.w_off = 0;
@@ -49,9 +50,9 @@ MixTmaCfg mix_tma_cfg(int B, int Cin, int Cout) {
     return c;
 }
 
-// Threads: OC x NBH.  Thread t handles output channel o0 + (t % OC) and batch
-// rows b0 + (t / OC) * BTT .. + BTT.
-template <int BTT>
+// Threads: (OC / OT) x NBH.  Thread t handles the OT output channels
+// o0 + (t % (OC/OT)) + j * (OC/OT) and batch rows b0 + (t / (OC/OT)) * BTT .. + BTT.
+template <int BTT, int OT>
 __global__ void __launch_bounds__(256)
 mix_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                float2* __restrict__ Z, int B, int Cin, int Cout, int NM, int OC, int IC, int BT,
@@ -60,7 +61,8 @@ mix_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     unsigned char* stages = smem + 128;
     const int tid = threadIdx.x;
-    const int ol = tid % OC, bh = tid / OC;
+    const int OS = OC / OT;  // stride between a thread's output channels
+    const int ol = tid % OS, bh = tid / OS;
     const int m0 = blockIdx.x * 4, o0 = blockIdx.y * OC, b0 = blockIdx.z * BT;
     const int nch = (Cin + IC - 1) / IC;
     const uint32_t w_bytes = 32u * OC * IC;
@@ -84,11 +86,13 @@ mix_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         }
     }
 
-    float2 acc[BTT][4];
+    float2 acc[OT][BTT][4];
 #pragma unroll
-    for (int bb = 0; bb < BTT; ++bb)
+    for (int j = 0; j < OT; ++j)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[bb][q] = make_float2(0.f, 0.f);
+        for (int bb = 0; bb < BTT; ++bb)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[j][bb][q] = make_float2(0.f, 0.f);
 
     // the two 16-byte halves of a thread's 32-byte w row are read in an order
     // that makes each quarter-warp touch 8 distinct 16-byte bank groups
@@ -108,19 +112,30 @@ mix_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         const float4* Xst = reinterpret_cast<const float4*>(st + w_bytes);  // [BT][IC][4 modes]
         const int ni = min(IC, Cin - c * IC);
         for (int ii = 0; ii < ni; ++ii) {
-            const float4* wrow = Wst + (ii * OC + ol) * 2;
-            const float4 p0 = wrow[h], p1 = wrow[1 - h];
-            const float4 lo = h ? p1 : p0, hi = h ? p0 : p1;
-            const float2 w0 = make_float2(lo.x, lo.y), w1 = make_float2(lo.z, lo.w);
-            const float2 w2 = make_float2(hi.x, hi.y), w3 = make_float2(hi.z, hi.w);
+            float2 w[OT][4];
+#pragma unroll
+            for (int j = 0; j < OT; ++j) {
+                const float4* wrow = Wst + (ii * OC + ol + j * OS) * 2;
+                const float4 p0 = wrow[h], p1 = wrow[1 - h];
+                const float4 lo = h ? p1 : p0, hi = h ? p0 : p1;
+                w[j][0] = make_float2(lo.x, lo.y);
+                w[j][1] = make_float2(lo.z, lo.w);
+                w[j][2] = make_float2(hi.x, hi.y);
+                w[j][3] = make_float2(hi.z, hi.w);
+            }
 #pragma unroll
             for (int bb = 0; bb < BTT; ++bb) {
                 const float4* xr = Xst + ((bh * BTT + bb) * IC + ii) * 2;
                 const float4 xa = xr[0], xb = xr[1];
-                cmac(acc[bb][0], make_float2(xa.x, xa.y), w0);
-                cmac(acc[bb][1], make_float2(xa.z, xa.w), w1);
-                cmac(acc[bb][2], make_float2(xb.x, xb.y), w2);
-                cmac(acc[bb][3], make_float2(xb.z, xb.w), w3);
+                const float2 x0 = make_float2(xa.x, xa.y), x1 = make_float2(xa.z, xa.w);
+                const float2 x2 = make_float2(xb.x, xb.y), x3 = make_float2(xb.z, xb.w);
+#pragma unroll
+                for (int j = 0; j < OT; ++j) {
+                    cmac(acc[j][bb][0], x0, w[j][0]);
+                    cmac(acc[j][bb][1], x1, w[j][1]);
+                    cmac(acc[j][bb][2], x2, w[j][2]);
+                    cmac(acc[j][bb][3], x3, w[j][3]);
+                }
             }
         }
         __syncthreads();  // every thread is done with stage s
@@ -141,23 +156,174 @@ mix_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         return;
     }
 
-    const int o = o0 + ol;
-    if (o >= Cout) return;
     const bool vec = (NM & 3) == 0 && m0 + 3 < NM;
 #pragma unroll
-    for (int bb = 0; bb < BTT; ++bb) {
-        const int b = b0 + bh * BTT + bb;
-        if (b >= B) break;
-        float2* zp = Z + ((size_t)b * Cout + o) * NM + m0;
-        if (vec) {
-            reinterpret_cast<float4*>(zp)[0] =
-                make_float4(acc[bb][0].x, acc[bb][0].y, acc[bb][1].x, acc[bb][1].y);
-            reinterpret_cast<float4*>(zp)[1] =
-                make_float4(acc[bb][2].x, acc[bb][2].y, acc[bb][3].x, acc[bb][3].y);
-        } else {
+    for (int j = 0; j < OT; ++j) {
+        const int o = o0 + ol + j * OS;
+        if (o >= Cout) break;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (m0 + q < NM) zp[q] = acc[bb][q];
+        for (int bb = 0; bb < BTT; ++bb) {
+            const int b = b0 + bh * BTT + bb;
+            if (b >= B) break;
+            float2* zp = Z + ((size_t)b * Cout + o) * NM + m0;
+            if (vec) {
+                reinterpret_cast<float4*>(zp)[0] =
+                    make_float4(acc[j][bb][0].x, acc[j][bb][0].y, acc[j][bb][1].x, acc[j][bb][1].y);
+                reinterpret_cast<float4*>(zp)[1] =
+                    make_float4(acc[j][bb][2].x, acc[j][bb][2].y, acc[j][bb][3].x, acc[j][bb][3].y);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (m0 + q < NM) zp[q] = acc[j][bb][q];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Register-tiled variant.  Each thread accumulates 4 output channels x BC
+// batch rows x 2 modes (8*BC complex accumulators), so every shared-memory
+// load feeds 8 or more FMAs.  A warp covers 8 channel groups x 4 batch groups
+// (or fewer batch groups when the batch is small): lanes with the same
+// channel group read the same w words and lanes with the same batch group the
+// same X words, which the hardware broadcasts.  Lanes are laid out as
+// (channel-group low bits: 4) x (mode half: 2) x (batch group) and each lane
+// walks its 4 channel rows starting at row (k + og) mod 4, so at every step
+// the 8 distinct 16-byte w chunks a warp reads lie in 8 different bank groups.
+struct MixTileCfg {
+    int OC, IC, BT, BC, NBG, threads;
+    size_t w_bytes, x_off, stage, smem;
+};
+
+__host__ __device__ inline size_t round1024(size_t v) { return (v + 1023) / 1024 * 1024; }
+
+MixTileCfg mix_tile_cfg(int B, int Cin, int Cout) {
+    MixTileCfg c;
+    c.OC = std::min(128, (Cout + 31) / 32 * 32);
+    int bt = 1;
+    while (bt < B && bt < 16) bt <<= 1;
+    c.BT = bt;
+    c.BC = std::min(bt, 4);
+    c.NBG = bt / c.BC;
+    c.threads = (c.OC / 4) * c.NBG * 2;
+    c.IC = std::max(1, std::min(Cin, 8192 / (32 * c.OC)));
+    c.w_bytes = (size_t)32 * c.OC * c.IC;
+    c.x_off = round1024(c.w_bytes);
+    c.stage = c.x_off + round1024((size_t)32 * c.IC * c.BT);
+    c.smem = 1024 + 1024 + (size_t)kStages * c.stage;  // barriers + alignment slack + ring
+    return c;
+}
+
+template <int BC>
+__global__ void __launch_bounds__(256)
+mix_tile_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                float2* __restrict__ Z, int B, int Cin, int Cout, int NM, int OC, int IC, int BT,
+                int NBG, unsigned* __restrict__ err) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+    // ring start aligned to 1 KB (the swizzle atom)
+    unsigned char* ring = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1024 + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    // thread -> (channel group og, batch group bg, mode half mh)
+    const int og_lo = tid & 3, mh = (tid >> 2) & 1, rest = tid >> 3;
+    const int bg = rest % NBG, og = og_lo + 4 * (rest / NBG);
+    const int m0 = blockIdx.x * 4, o0 = blockIdx.y * OC, b0 = blockIdx.z * BT;
+    const int nch = (Cin + IC - 1) / IC;
+    const uint32_t w_bytes = 32u * OC * IC;
+    const uint32_t x_off = (w_bytes + 1023u) & ~1023u;
+    const uint32_t x_bytes = 32u * IC * BT;
+    const uint32_t stage = x_off + ((x_bytes + 1023u) & ~1023u);
+    const uint32_t tx = w_bytes + x_bytes;
+
+    if (tid == 0) {
+        prefetch_tensormap(&tmW);
+        prefetch_tensormap(&tmX);
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    int issued = 0;
+    if (tid == 0) {
+        for (; issued < kStages && issued < nch; ++issued) {
+            unsigned char* st = ring + (size_t)issued * stage;
+            mbar_arrive_expect_tx(&bars[issued], tx);
+            tma_load_3d(st, &tmW, 2 * m0, o0, issued * IC, &bars[issued]);
+            tma_load_3d(st + x_off, &tmX, 2 * m0, issued * IC, b0, &bars[issued]);
+        }
+    }
+
+    float2 acc[4][BC][2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int bb = 0; bb < BC; ++bb) acc[j][bb][0] = acc[j][bb][1] = make_float2(0.f, 0.f);
+
+    int consumed = 0;
+    bool timed_out = false;
+    for (int c = 0; c < nch; ++c) {
+        const int s = c % kStages;
+        const bool ok = wait_parity_bounded(&bars[s], (uint32_t)((c / kStages) & 1), err);
+        if (__syncthreads_or(!ok)) {
+            timed_out = true;
+            break;
+        }
+        consumed = c + 1;
+        const unsigned char* st = ring + (size_t)s * stage;
+        const int ni = min(IC, Cin - c * IC);
+        for (int ii = 0; ii < ni; ++ii) {
+            float4 w[4], xv[BC];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {  // w[k] is channel row (k + og) mod 4
+                const uint32_t off = (uint32_t)((ii * OC + og * 4 + ((k + og_lo) & 3)) * 32 + 16 * mh);
+                w[k] = *reinterpret_cast<const float4*>(st + off);
+            }
+#pragma unroll
+            for (int bb = 0; bb < BC; ++bb) {
+                const uint32_t off = (uint32_t)(((bg * BC + bb) * IC + ii) * 32 + 16 * mh);
+                xv[bb] = *reinterpret_cast<const float4*>(st + x_off + off);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int bb = 0; bb < BC; ++bb) {
+                    cmac(acc[j][bb][0], make_float2(xv[bb].x, xv[bb].y), make_float2(w[j].x, w[j].y));
+                    cmac(acc[j][bb][1], make_float2(xv[bb].z, xv[bb].w), make_float2(w[j].z, w[j].w));
+                }
+        }
+        __syncthreads();
+        if (tid == 0 && issued < nch) {
+            unsigned char* st2 = ring + (size_t)s * stage;
+            mbar_arrive_expect_tx(&bars[s], tx);
+            tma_load_3d(st2, &tmW, 2 * m0, o0, issued * IC, &bars[s]);
+            tma_load_3d(st2 + x_off, &tmX, 2 * m0, issued * IC, b0, &bars[s]);
+            ++issued;
+        }
+    }
+    if (timed_out) {
+        if (tid == 0)
+            for (int c = consumed; c < issued; ++c)
+                wait_parity_bounded(&bars[c % kStages], (uint32_t)((c / kStages) & 1), err);
+        __syncthreads();
+        return;
+    }
+    const int m = m0 + 2 * mh;
+    if (m >= NM) return;
+    const bool pair = m + 1 < NM;  // NM is even, so this always holds; kept for safety
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int o = o0 + og * 4 + ((j + og_lo) & 3);
+        if (o >= Cout) continue;
+#pragma unroll
+        for (int bb = 0; bb < BC; ++bb) {
+            const int b = b0 + bg * BC + bb;
+            if (b >= B) break;
+            float2* zp = Z + ((size_t)b * Cout + o) * NM + m;
+            if (pair)
+                *reinterpret_cast<float4*>(zp) =
+                    make_float4(acc[j][bb][0].x, acc[j][bb][0].y, acc[j][bb][1].x, acc[j][bb][1].y);
+            else
+                zp[0] = acc[j][bb][0];
         }
     }
 }
@@ -166,15 +332,30 @@ template <int BTT>
 cudaError_t launch_btt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, int B, int Cin,
                        int Cout, int NM, const MixTmaCfg& c, unsigned* err, cudaStream_t s) {
     dim3 grid((NM + 3) / 4, (Cout + c.OC - 1) / c.OC, (B + c.BT - 1) / c.BT);
-    mix_tma_kernel<BTT><<<grid, c.OC * c.NBH, c.smem, s>>>(mw, mx, Z, B, Cin, Cout, NM, c.OC,
-                                                          c.IC, c.BT, err);
+    const int threads = c.OC / c.OT * c.NBH;
+    if (c.OT == 2)
+        mix_tma_kernel<BTT, 2><<<grid, threads, c.smem, s>>>(mw, mx, Z, B, Cin, Cout, NM, c.OC,
+                                                             c.IC, c.BT, err);
+    else
+        mix_tma_kernel<BTT, 1><<<grid, threads, c.smem, s>>>(mw, mx, Z, B, Cin, Cout, NM, c.OC,
+                                                             c.IC, c.BT, err);
     return cudaGetLastError();
+}
+
+template <int BC>
+cudaError_t set_attr_tile() {
+    return cudaFuncSetAttribute(mix_tile_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                227 * 1024);
 }
 
 template <int BTT>
 cudaError_t set_attr() {
-    return cudaFuncSetAttribute(mix_tma_kernel<BTT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(mix_tma_kernel<BTT, 1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mix_tma_kernel<BTT, 2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    return e;
 }
 
 }  // namespace
@@ -200,6 +381,9 @@ cudaError_t mix_tma_init() {
     if (e == cudaSuccess) e = set_attr<2>();
     if (e == cudaSuccess) e = set_attr<4>();
     if (e == cudaSuccess) e = set_attr<8>();
+    if (e == cudaSuccess) e = set_attr_tile<1>();
+    if (e == cudaSuccess) e = set_attr_tile<2>();
+    if (e == cudaSuccess) e = set_attr_tile<4>();
     if (e == cudaSuccess && !fno_get_encode_tiled()) e = cudaErrorNotSupported;
     return e;
 }
@@ -213,7 +397,8 @@ bool mix_tma_supported(int B, int Cin, int Cout, int nm) {
 // dims (2*NM, d1, d2), box (8 floats = 4 modes, b1, b2).  Out-of-range box
 // elements are filled with zeros.
 static bool encode_modes_map(CUtensorMap* map, const float2* base, int NM, int d1, int d2,
-                             int b1, int b2) {
+                             int b1, int b2,
+                             CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
     fno_encode_tiled_fn enc = fno_get_encode_tiled();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)NM * 2, (cuuint64_t)d1, (cuuint64_t)d2};
@@ -221,13 +406,34 @@ static bool encode_modes_map(CUtensorMap* map, const float2* base, int NM, int d
     cuuint32_t box[3] = {8, (cuuint32_t)b1, (cuuint32_t)b2};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float2*>(base), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
+static bool use_tile(int B, int Cin, int Cout) {
+    const MixTileCfg t = mix_tile_cfg(B, Cin, Cout);
+    return t.threads >= 64 && t.smem <= 227 * 1024;
+}
+
 cudaError_t launch_mix_tma(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                            cudaStream_t s, fno_launch_ctx* ctx) {
+    if (use_tile(p.B, p.Cin, p.Cout)) {
+        const MixTileCfg t = mix_tile_cfg(p.B, p.Cin, p.Cout);
+        CUtensorMap mw, mx;
+        if (!encode_modes_map(&mw, w, p.nm, p.Cout, p.Cin, t.OC, t.IC) ||
+            !encode_modes_map(&mx, X, p.nm, p.Cin, p.B, t.IC, t.BT))
+            return cudaErrorInvalidValue;
+        dim3 grid((p.nm + 3) / 4, (p.Cout + t.OC - 1) / t.OC, (p.B + t.BT - 1) / t.BT);
+        switch (t.BC) {
+            case 1: mix_tile_kernel<1><<<grid, t.threads, t.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, t.OC, t.IC, t.BT, t.NBG, p.err); break;
+            case 2: mix_tile_kernel<2><<<grid, t.threads, t.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, t.OC, t.IC, t.BT, t.NBG, p.err); break;
+            default: mix_tile_kernel<4><<<grid, t.threads, t.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, t.OC, t.IC, t.BT, t.NBG, p.err); break;
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess && ctx) e = ctx->mark(s);
+        return e;
+    }
     const MixTmaCfg c = mix_tma_cfg(p.B, p.Cin, p.Cout);
     CUtensorMap mw, mx;
     if (!encode_modes_map(&mw, w, p.nm, p.Cout, p.Cin, c.OC, c.IC) ||

@@ -1,0 +1,349 @@
+// stages_big.cu -- fused transform kernels for long rows, W in {512, 1024,
+// 2048, 4096}, with at most 64 kept columns (m2 <= 64).
+//
+// A CTA (256 threads) owns the R rows h = p + P*q of one plane, like the
+// short-row kernels, and shares their column halves (fused_columns.cuh).  A row
+// pair is handled by a group of L = W/16 threads (L in {32..256}):
+//
+// Forward row transform of the packed pair z = x_a + i x_b, pruned to the bins
+// k < m2 and k > W - m2 (decimation in frequency, W = 16 * L):
+//   pass 1: thread n1 < L loads z[n1 + L*n2] (n2 < 16; consecutive threads read
+//           consecutive words), 16-point register DFT over n2, times
+//           e^{-2 pi i n1 kk / W}, stored as S[kk][n1];
+//   pass 2: for each kk, the L-point DFT over n1 is needed only at the few
+//           k1 with 16*k1 + kk kept.  With n1 = a + G*b (G = L/16 lanes, b < 16),
+//             Zk[k1] = sum_a e^{-2 pi i a k1 / L} D_a[k1 mod 16],
+//             D_a[d] = 16-point DFT over b of S[kk][a + G*b];
+//           thread (kk, a) computes D_a, forms its terms for every candidate k1
+//           and the G lanes of a kk sum them with a shuffle reduce-scatter.
+//   The kept bins meet in shared memory and are separated into the two rows'
+//   spectra exactly as in the short-row kernels.
+// Inverse (complex-to-real) row transform: the exact mirror (decimation in
+// time), the kept bins of U = S_a + i S_b entering as the only nonzero inputs.
+#include <algorithm>
+
+#include "fft_reg.cuh"
+#include "fused_columns.cuh"
+#include "internal.h"
+
+namespace fno {
+namespace {
+
+constexpr int kBT = 256;      // threads per CTA
+constexpr int kNL = 4;        // candidate k1 per side: ceil(m2 / 16) <= 4, i.e. m2 <= 64
+
+template <int W>
+struct BigCfg {
+    static constexpr int L = W / 16;               // threads per row pair
+    static constexpr int G = L / 16;               // lanes reduced per bin kk
+    static constexpr int NK = 2 * kNL > G ? 2 * kNL : G;  // candidate slots per kk
+    static constexpr int Groups = kBT / L;
+    static constexpr int SStride = L + G;          // S row stride (== G mod 16)
+    static constexpr int GroupScr = 16 * SStride + 16 * NK;
+};
+
+template <int W, int R>
+struct BigKCfg {
+    static constexpr int Scratch = BigCfg<W>::Groups * BigCfg<W>::GroupScr > ColCfg<R>::Scratch
+                                       ? BigCfg<W>::Groups * BigCfg<W>::GroupScr
+                                       : ColCfg<R>::Scratch;
+};
+
+template <int W, int R>
+size_t big_smem_bytes(int m2) {
+    return sizeof(float2) * ((size_t)BigKCfg<W, R>::Scratch + (size_t)R * (m2 + 1));
+}
+
+// Synchronise the L threads of a row-pair group.
+template <int L>
+__device__ __forceinline__ void group_sync(int g) {
+    if constexpr (L <= 32) {
+        __syncwarp();
+    } else if constexpr (L == kBT) {
+        __syncthreads();
+    } else {
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(L) : "memory");
+    }
+}
+
+// Candidate k1 of slot j: the lower side 0..3, then the upper side L-4..L-1
+// (every bin k < 64 and k > W - 64); slots past 8 are unused.  Candidates
+// whose bin is not kept contribute zeros.
+template <int L>
+__device__ __forceinline__ constexpr int cand_k1(int j) { return j < kNL ? j : L - 2 * kNL + j; }
+
+// Reduce-scatter of N complex values over the G lanes (lane bits below G) that
+// share a bin: afterwards lane a holds the sums of slots a*N/G .. a*N/G + N/G - 1
+// in r[0 .. N/G).
+template <int N, int G>
+__device__ __forceinline__ void reduce_scatter(float2 (&r)[N], int a) {
+#pragma unroll
+    for (int s = G / 2, c = N; s >= 1; s >>= 1, c >>= 1) {
+        const bool up = (a & s) != 0;
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            if (i < c / 2) {
+                const float2 lo = r[i], hi = r[i + c / 2];
+                const float2 send = up ? lo : hi;
+                const float2 keep = up ? hi : lo;
+                float2 recv;
+                recv.x = __shfl_xor_sync(0xffffffffu, send.x, s);
+                recv.y = __shfl_xor_sync(0xffffffffu, send.y, s);
+                r[i] = cadd(keep, recv);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- forward ---
+template <int W, int R>
+__global__ void __launch_bounds__(kBT, 2)
+fwd_big_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m1, int m2, int P,
+               float scale, const float2* __restrict__ tw_w, const float2* __restrict__ tw_h) {
+    using B = BigCfg<W>;
+    constexpr int L = B::L, G = B::G, NK = B::NK;
+    extern __shared__ float2 sm[];
+    float2* scr = sm;
+    float2* Y = sm + BigKCfg<W, R>::Scratch;  // [R][ys]
+    const int ys = m2 + 1;
+    const int plane = blockIdx.x / P;
+    const int p = blockIdx.x - plane * P;
+    const float* xp = x + (size_t)plane * H * W;
+
+    const int g = threadIdx.x / L, t = threadIdx.x % L;
+    float2* S = scr + g * B::GroupScr;  // S[kk][n1], row stride L + G
+    float2* Zs = S + 16 * B::SStride;   // Zs[kk][slot]
+    // pass-1 twiddles e^{-2 pi i n1 kk / W} for n1 = t, and pass-2 twiddles
+    // e^{-2 pi i a k1 / L} = e^{-2 pi i 16 a k1 / W} for the candidate k1
+    const int kk2 = t / G, a = t % G;
+    float2 tw1[16], tw2[NK];
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) tw1[kk] = root<-1>(tw_w, t * kk, W);
+#pragma unroll
+    for (int j = 0; j < NK; ++j) tw2[j] = root<-1>(tw_w, 16 * a * cand_k1<L>(j), W);
+
+    constexpr int npairs = R / 2;
+    constexpr int iters = (npairs + B::Groups - 1) / B::Groups;
+    for (int it = 0; it < iters; ++it) {
+        const int pair = g + it * B::Groups;
+        const bool active = pair < npairs;  // uniform over the group
+        const int qa = 2 * pair;
+        if (active) {
+            const float* ra = xp + (size_t)(p + P * qa) * W;
+            const float* rb = ra + (size_t)P * W;
+            float2 v[16];
+#pragma unroll
+            for (int n2 = 0; n2 < 16; ++n2)
+                v[n2] = make_float2(__ldg(ra + t + L * n2), __ldg(rb + t + L * n2));
+            dft<16, -1>(v);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                S[kk * B::SStride + t] = kk == 0 ? v[0] : cmul(v[kk], tw1[kk]);
+        }
+        group_sync<L>(g);
+        if (active) {
+            float2 d[16];
+#pragma unroll
+            for (int b = 0; b < 16; ++b) d[b] = S[kk2 * B::SStride + a + G * b];
+            dft<16, -1>(d);
+            float2 r[NK];
+#pragma unroll
+            for (int j = 0; j < NK; ++j) {
+                const int k1 = cand_k1<L>(j);
+                r[j] = j < 2 * kNL ? cmul(d[k1 & 15], tw2[j]) : make_float2(0.f, 0.f);
+            }
+            reduce_scatter<NK, G>(r, a);
+#pragma unroll
+            for (int j = 0; j < NK / G; ++j) Zs[kk2 * NK + a * (NK / G) + j] = r[j];
+        }
+        group_sync<L>(g);
+        if (active) {
+            // separation of the two rows' spectra for k = 16*k1 + kk < m2
+            for (int k = t; k < m2; k += L) {
+                const int kk = k & 15, k1 = k >> 4;  // k1 < NL: lower slot k1
+                const float2 zk = Zs[kk * NK + k1];
+                float2 zm;  // Z[W - k]
+                if (kk == 0) {
+                    zm = k1 == 0 ? Zs[0] : Zs[0 * NK + (L - k1) - L + 2 * kNL];
+                } else {
+                    zm = Zs[(16 - kk) * NK + (L - 1 - k1) - L + 2 * kNL];
+                }
+                Y[qa * ys + k] = make_float2(0.5f * (zk.x + zm.x), 0.5f * (zk.y - zm.y));
+                Y[(qa + 1) * ys + k] = make_float2(0.5f * (zk.y + zm.y), -0.5f * (zk.x - zm.x));
+            }
+        }
+        // the next pair's pass 1 rewrites S only; S was last read before the
+        // second barrier above, and Zs is rewritten only after the next first barrier
+    }
+    __syncthreads();
+    columns_forward<R>(scr, Y, ys, X, (size_t)plane * 2 * m1 * m2, H, m1, m2, P, p, scale, tw_h);
+}
+
+// ---------------------------------------------------------------- inverse ---
+template <int W, int R>
+__global__ void __launch_bounds__(kBT, 2)
+inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m1, int m2, int P,
+               float scale, const float2* __restrict__ tw_w, const float2* __restrict__ tw_h) {
+    using B = BigCfg<W>;
+    constexpr int L = B::L, G = B::G, NK = B::NK;
+    constexpr int half = W / 2;
+    extern __shared__ float2 sm[];
+    float2* scr = sm;
+    float2* V = sm + BigKCfg<W, R>::Scratch;  // [R][ys]
+    const int ys = m2 + 1;
+    const int plane = blockIdx.x / P;
+    const int p = blockIdx.x - plane * P;
+    const float2* Zp = Z + (size_t)plane * 2 * m1 * m2;
+
+    columns_inverse<R>(scr, V, ys, Zp, H, m1, m2, P, p, tw_h);
+    __syncthreads();
+
+    const int g = threadIdx.x / L, t = threadIdx.x % L;
+    float2* S = scr + g * B::GroupScr;  // S[kk][n1], row stride L + G
+    const int kk2 = t / G, a = t % G;
+    float2 tw1[16], tw2[NK];
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) tw1[kk] = root<1>(tw_w, t * kk, W);
+#pragma unroll
+    for (int j = 0; j < NK; ++j) tw2[j] = root<1>(tw_w, 16 * a * cand_k1<L>(j), W);
+    float* yp = y + (size_t)plane * H * W;
+
+    constexpr int npairs = R / 2;
+    constexpr int iters = (npairs + B::Groups - 1) / B::Groups;
+    for (int it = 0; it < iters; ++it) {
+        const int pair = g + it * B::Groups;
+        const bool active = pair < npairs;
+        const int qa = 2 * pair;
+        if (active) {
+            const float2* Va = V + qa * ys;
+            const float2* Vb = Va + ys;
+            // E_a[d] = sum over candidates k1 == d (mod 16) of e^{+2 pi i a k1 / L} U[16 k1 + kk]
+            float2 e[16];
+#pragma unroll
+            for (int d = 0; d < 16; ++d) e[d] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 2 * kNL; ++j) {
+                const int k1 = cand_k1<L>(j);
+                const int k = 16 * k1 + kk2;
+                const int kr = k <= half ? k : W - k;
+                if (kr >= m2) continue;
+                float2 uk, um;
+                packed_bin(Va[kr], Vb[kr], kr == 0 || kr == half, &uk, &um);
+                const float2 u = k <= half ? uk : um;
+                e[k1 & 15] = cmul(u, tw2[j]);
+            }
+            dft<16, 1>(e);
+#pragma unroll
+            for (int b = 0; b < 16; ++b) S[kk2 * B::SStride + a + G * b] = e[b];
+        }
+        group_sync<L>(g);
+        if (active) {
+            float2 v[16];
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                v[kk] = kk == 0 ? S[t] : cmul(S[kk * B::SStride + t], tw1[kk]);
+            dft<16, 1>(v);
+            float* ya = yp + (size_t)(p + P * qa) * W;
+            float* yb = ya + (size_t)P * W;
+#pragma unroll
+            for (int n2 = 0; n2 < 16; ++n2) {
+                ya[t + L * n2] = v[n2].x * scale;
+                yb[t + L * n2] = v[n2].y * scale;
+            }
+        }
+        group_sync<L>(g);
+    }
+}
+
+template <int W, int R>
+cudaError_t set_attrs() {
+    const int bytes = (int)std::min<size_t>(big_smem_bytes<W, R>(64), 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(fwd_big_kernel<W, R>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inv_big_kernel<W, R>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e;
+}
+
+template <int W>
+cudaError_t set_attrs_w() {
+    cudaError_t e = set_attrs<W, 32>();
+    if (e == cudaSuccess) e = set_attrs<W, 64>();
+    if (e == cudaSuccess) e = set_attrs<W, 128>();
+    if (e == cudaSuccess) e = set_attrs<W, 256>();
+    return e;
+}
+
+template <bool FWD, int W, int R>
+cudaError_t launch(const fno_plan_s& p, const float* x, float2* X, const float2* Z, float* y,
+                   cudaStream_t s) {
+    const size_t smem = big_smem_bytes<W, R>(p.m2);
+    if (FWD) {
+        const unsigned grid = (unsigned)((size_t)p.B * p.Cin * p.P);
+        fwd_big_kernel<W, R><<<grid, kBT, smem, s>>>(x, X, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
+                                                     p.tw_h);
+    } else {
+        const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.P);
+        inv_big_kernel<W, R><<<grid, kBT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
+                                                     p.tw_h);
+    }
+    return cudaGetLastError();
+}
+
+template <bool FWD, int W>
+cudaError_t dispatch_r(const fno_plan_s& p, const float* x, float2* X, const float2* Z, float* y,
+                       cudaStream_t s) {
+    switch (p.R) {
+        case 32: return launch<FWD, W, 32>(p, x, X, Z, y, s);
+        case 64: return launch<FWD, W, 64>(p, x, X, Z, y, s);
+        case 128: return launch<FWD, W, 128>(p, x, X, Z, y, s);
+        case 256: return launch<FWD, W, 256>(p, x, X, Z, y, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <bool FWD>
+cudaError_t dispatch(const fno_plan_s& p, const float* x, float2* X, const float2* Z, float* y,
+                     cudaStream_t s) {
+    switch (p.W) {
+        case 512: return dispatch_r<FWD, 512>(p, x, X, Z, y, s);
+        case 1024: return dispatch_r<FWD, 1024>(p, x, X, Z, y, s);
+        case 2048: return dispatch_r<FWD, 2048>(p, x, X, Z, y, s);
+        case 4096: return dispatch_r<FWD, 4096>(p, x, X, Z, y, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace fno
+
+using namespace fno;
+
+cudaError_t stages_big_init() {
+    cudaError_t e = set_attrs_w<512>();
+    if (e == cudaSuccess) e = set_attrs_w<1024>();
+    if (e == cudaSuccess) e = set_attrs_w<2048>();
+    if (e == cudaSuccess) e = set_attrs_w<4096>();
+    return e;
+}
+
+size_t big_smem_bytes_any(int W, int R, int m2) {
+    switch (W * 1000 + R) {
+#define CASE(w, r) case w * 1000 + r: return big_smem_bytes<w, r>(m2);
+        CASE(512, 32) CASE(512, 64) CASE(512, 128) CASE(512, 256)
+        CASE(1024, 32) CASE(1024, 64) CASE(1024, 128) CASE(1024, 256)
+        CASE(2048, 32) CASE(2048, 64) CASE(2048, 128) CASE(2048, 256)
+        CASE(4096, 32) CASE(4096, 64) CASE(4096, 128) CASE(4096, 256)
+#undef CASE
+    }
+    return (size_t)-1;
+}
+
+cudaError_t launch_forward_big(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s) {
+    return dispatch<true>(p, x, X, nullptr, nullptr, s);
+}
+
+cudaError_t launch_inverse_big(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s) {
+    return dispatch<false>(p, nullptr, nullptr, Z, y, s);
+}

@@ -33,6 +33,7 @@
 #include <algorithm>
 
 #include "fft_reg.cuh"
+#include "fused_columns.cuh"
 #include "internal.h"
 
 namespace fno {
@@ -40,21 +41,35 @@ namespace {
 
 constexpr int kFT = 256;  // threads per CTA
 
+// Row-pass scratch of one row-pair group: forward S[kk][n1] (row stride Bq+1),
+// inverse S[n1][kk] (row stride 17), plus for Bq = 16 the W outputs of the
+// pair.  The group stride is == Bq (mod 16) complex elements so that the
+// 16/Bq groups sharing a half-warp fall on different shared-memory banks.
+template <int W>
+struct RowCfg {
+    static constexpr int Bq = W / 16;
+    static constexpr int need0 = 16 * (Bq + 1) > 17 * Bq ? 16 * (Bq + 1) : 17 * Bq;
+    static constexpr int need = need0 + (Bq == 16 ? W : 0);
+    static constexpr int Scr = need + ((Bq % 16) - need % 16 + 16) % 16;
+};
+
 template <int W, int R>
 struct FusedCfg {
     static constexpr int BqW = W / 16;           // threads per row pair
     static constexpr int BqR = R / 16;           // threads per column
     static constexpr int RowGroups = kFT / BqW;  // row pairs in flight
     static constexpr int ColsPerPass = kFT / BqR;
-    // Row-pass scratch per group: S[kk][n1] with row stride Bq+1; the group
-    // stride is 1 mod 16 complex so that neighbouring groups use other banks.
-    static constexpr int RowStride = BqW + 1;
-    static constexpr int RowScr = ((16 * RowStride + W + 15) / 16) * 16 + 1;
-    // Column-pass scratch: S[col][kk][n1], per column stride R + 16 + 1.
+    static_assert(kFT == kColThreads, "column passes assume 256 threads");
+    static constexpr int RowScr = RowCfg<W>::Scr;
+    // Column-pass scratch: S[col][kk][n1], per column stride R + 17 (== 1 mod 16,
+    // lanes run over columns).
     static constexpr int ColScr = R + 17;
     static constexpr int ScratchA = RowGroups * RowScr;
     static constexpr int ScratchB = ColsPerPass * ColScr;
     static constexpr int Scratch = ScratchA > ScratchB ? ScratchA : ScratchB;
+    // CTAs per SM the register allocation is sized for (shared memory allows
+    // three for planes up to 128 x 128, fewer above)
+    static constexpr int MinBlocks = W * R <= 128 * 128 ? 3 : (W * R <= 256 * 128 ? 2 : 1);
 };
 
 template <int W, int R>
@@ -63,9 +78,193 @@ size_t fused_smem_bytes(int m2) {
     return sizeof(float2) * ((size_t)C::Scratch + (size_t)R * (m2 + 1));
 }
 
+// Mirror partner of bin kk of the 16-point first pass: kk and (16 - kk) mod 16
+// are handled by the same thread so that Z[k] and Z[W - k] meet in registers.
+// Pair p (p in [0, 8)) is {0, 8} for p = 0 and {p, 16 - p} otherwise.
+__device__ __forceinline__ int pair_a(int p) { return p; }
+__device__ __forceinline__ int pair_b(int p) { return p == 0 ? 8 : 16 - p; }
+
+// One packed row pair through the forward row transform.  Called by every lane
+// of the warp (the group of Bq lanes is inside one warp); `active` lanes do work.
+// Writes the separated spectra of the two rows, bins k < m2, to Ya and Yb.
+template <int W>
+__device__ __forceinline__ void row_pair_forward(const float* __restrict__ ra,
+                                                 const float* __restrict__ rb, float2* S,
+                                                 float2* Ya, float2* Yb, int t, int m2,
+                                                 const float2* __restrict__ tw, bool active) {
+    constexpr int Bq = W / 16;
+    constexpr int RS = Bq + 1;
+    if (active) {
+        float2 v[16];
+#pragma unroll
+        for (int n2 = 0; n2 < 16; ++n2)
+            v[n2] = make_float2(__ldg(ra + t + Bq * n2), __ldg(rb + t + Bq * n2));
+        dft<16, -1>(v);
+#pragma unroll
+        for (int kk = 1; kk < 16; ++kk) v[kk] = cmul(v[kk], root<-1>(tw, t * kk, W));
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) S[kk * RS + t] = v[kk];
+    }
+    __syncwarp();
+    if constexpr (Bq == 16) {
+        // one bin kk = t per thread; the outputs meet in shared memory
+        float2* Zs = S + 16 * RS;
+        if (active) {
+            float2 u[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) u[j] = S[t * RS + j];
+            dft<16, -1>(u);
+#pragma unroll
+            for (int k1 = 0; k1 < 16; ++k1) {
+                const int k = 16 * k1 + t;
+                if (k < m2 || k > W - m2) Zs[k] = u[k1];
+            }
+        }
+        __syncwarp();
+        if (active) {
+            for (int k = t; k < m2; k += Bq) {
+                const float2 zk = Zs[k], zm = Zs[(W - k) & (W - 1)];
+                Ya[k] = make_float2(0.5f * (zk.x + zm.x), 0.5f * (zk.y - zm.y));
+                Yb[k] = make_float2(0.5f * (zk.y + zm.y), -0.5f * (zk.x - zm.x));
+            }
+        }
+        __syncwarp();
+    } else {
+        constexpr int NP = 8 / Bq;  // mirror pairs per thread
+        float2 za[NP][Bq], zb[NP][Bq];
+        if (active) {
+#pragma unroll
+            for (int ps = 0; ps < NP; ++ps) {
+                const int p = t + Bq * ps;
+                const int ka = pair_a(p), kb = pair_b(p);
+#pragma unroll
+                for (int j = 0; j < Bq; ++j) {
+                    za[ps][j] = S[ka * RS + j];
+                    zb[ps][j] = S[kb * RS + j];
+                }
+                dft<Bq, -1>(za[ps]);
+                dft<Bq, -1>(zb[ps]);
+            }
+        }
+        __syncwarp();  // S may be overwritten by the next pair from here on
+        if (active) {
+#pragma unroll
+            for (int ps = 0; ps < NP; ++ps) {
+                const int p = t + Bq * ps;
+                const int ka = pair_a(p), kb = pair_b(p);
+#pragma unroll
+                for (int k1 = 0; k1 < Bq; ++k1) {
+                    // X_a[k] = (Z[k] + conj Z[W-k]) / 2,  X_b[k] = (Z[k] - conj Z[W-k]) / 2i
+                    const int k = 16 * k1 + ka;
+                    if (k < m2) {
+                        const float2 zk = za[ps][k1];
+                        const float2 zm = p == 0 ? za[ps][(Bq - k1) % Bq] : zb[ps][Bq - 1 - k1];
+                        Ya[k] = make_float2(0.5f * (zk.x + zm.x), 0.5f * (zk.y - zm.y));
+                        Yb[k] = make_float2(0.5f * (zk.y + zm.y), -0.5f * (zk.x - zm.x));
+                    }
+                    const int k2 = 16 * k1 + kb;
+                    if (k2 < m2) {
+                        const float2 zk = zb[ps][k1];
+                        const float2 zm = p == 0 ? zb[ps][Bq - 1 - k1] : za[ps][Bq - 1 - k1];
+                        Ya[k2] = make_float2(0.5f * (zk.x + zm.x), 0.5f * (zk.y - zm.y));
+                        Yb[k2] = make_float2(0.5f * (zk.y + zm.y), -0.5f * (zk.x - zm.x));
+                    }
+                }
+            }
+        }
+    }
+}
+
+// One row pair through the inverse (complex-to-real) row transform: reads the
+// kept bins of rows a and b from Va, Vb and writes the two output rows.
+template <int W>
+__device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2* Vb, float2* S,
+                                                 float* __restrict__ ya, float* __restrict__ yb,
+                                                 int t, int m2, const float2* __restrict__ tw,
+                                                 float scale, bool active) {
+    constexpr int Bq = W / 16;
+    constexpr int RS = 17;
+    constexpr int half = W / 2;
+    if (active) {
+        if constexpr (Bq == 16) {
+            const int kk = t;
+            float2 u[16];
+#pragma unroll
+            for (int k1 = 0; k1 < 16; ++k1) {
+                const int k = 16 * k1 + kk;
+                float2 val = make_float2(0.f, 0.f);
+                const int kr = k <= half ? k : W - k;
+                if (kr < m2) {
+                    float2 uk, um;
+                    packed_bin(Va[kr], Vb[kr], kr == 0 || kr == half, &uk, &um);
+                    val = k <= half ? uk : um;
+                }
+                u[k1] = val;
+            }
+            dft<16, 1>(u);
+#pragma unroll
+            for (int n1 = 0; n1 < 16; ++n1)
+                S[n1 * RS + kk] = n1 == 0 ? u[0] : cmul(u[n1], root<1>(tw, n1 * kk, W));
+        } else {
+            constexpr int NP = 8 / Bq;
+#pragma unroll
+            for (int ps = 0; ps < NP; ++ps) {
+                const int p = t + Bq * ps;
+                const int ka = pair_a(p), kb = pair_b(p);
+                float2 ua[Bq], ub[Bq];
+#pragma unroll
+                for (int j = 0; j < Bq; ++j) ua[j] = ub[j] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k1 = 0; k1 < Bq; ++k1) {
+                    const int k = 16 * k1 + ka;  // its mirror W - k is bin kb (ka if p = 0)
+                    if (k <= half && k < m2) {
+                        float2 uk, um;
+                        packed_bin(Va[k], Vb[k], k == 0 || k == half, &uk, &um);
+                        ua[k1] = uk;
+                        if (k != 0 && k != half) {
+                            if (p == 0) ua[(Bq - k1) % Bq] = um;
+                            else ub[Bq - 1 - k1] = um;
+                        }
+                    }
+                    const int k2 = 16 * k1 + kb;
+                    if (k2 <= half && k2 < m2) {
+                        float2 uk, um;
+                        packed_bin(Va[k2], Vb[k2], k2 == half, &uk, &um);
+                        ub[k1] = uk;
+                        if (k2 != half) {
+                            if (p == 0) ub[Bq - 1 - k1] = um;
+                            else ua[Bq - 1 - k1] = um;
+                        }
+                    }
+                }
+                dft<Bq, 1>(ua);
+                dft<Bq, 1>(ub);
+#pragma unroll
+                for (int n1 = 0; n1 < Bq; ++n1) {
+                    S[n1 * RS + ka] = n1 == 0 ? ua[0] : cmul(ua[n1], root<1>(tw, n1 * ka, W));
+                    S[n1 * RS + kb] = n1 == 0 ? ub[0] : cmul(ub[n1], root<1>(tw, n1 * kb, W));
+                }
+            }
+        }
+    }
+    __syncwarp();
+    if (active) {
+        float2 v[16];
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) v[kk] = S[t * RS + kk];
+        dft<16, 1>(v);
+#pragma unroll
+        for (int n2 = 0; n2 < 16; ++n2) {
+            ya[t + Bq * n2] = v[n2].x * scale;
+            yb[t + Bq * n2] = v[n2].y * scale;
+        }
+    }
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------- forward ---
 template <int W, int R>
-__global__ void __launch_bounds__(kFT)
+__global__ void __launch_bounds__(kFT, (FusedCfg<W, R>::MinBlocks))
 fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m1, int m2,
                  int P, float scale, const float2* __restrict__ tw_w,
                  const float2* __restrict__ tw_h) {
@@ -81,119 +280,28 @@ fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int
     // ---- rows -----------------------------------------------------------
     {
         constexpr int Bq = C::BqW;
-        constexpr int J = 16 / Bq;
-        const int g = threadIdx.x / Bq, n1 = threadIdx.x % Bq;
+        const int g = threadIdx.x / Bq, t = threadIdx.x % Bq;
         float2* S = scr + g * C::RowScr;
-        float2* Zs = S + 16 * C::RowStride;  // W kept outputs of this pair
         constexpr int npairs = R / 2;
         constexpr int iters = (npairs + C::RowGroups - 1) / C::RowGroups;
         for (int it = 0; it < iters; ++it) {
             const int pair = g + it * C::RowGroups;
             const bool active = pair < npairs;
             const int qa = 2 * pair;
-            if (active) {
-                const float* ra = xp + (size_t)(p + P * qa) * W;
-                const float* rb = xp + (size_t)(p + P * (qa + 1)) * W;
-                float2 v[16];
-#pragma unroll
-                for (int n2 = 0; n2 < 16; ++n2)
-                    v[n2] = make_float2(__ldg(ra + n1 + Bq * n2), __ldg(rb + n1 + Bq * n2));
-                dft<16, -1>(v);
-#pragma unroll
-                for (int kk = 1; kk < 16; ++kk) v[kk] = cmul(v[kk], root<-1>(tw_w, n1 * kk, W));
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) S[kk * C::RowStride + n1] = v[kk];
-            }
-            __syncwarp();
-            float2 u[J][Bq];
-            if (active) {
-#pragma unroll
-                for (int j = 0; j < J; ++j) {
-                    const int kk = n1 + Bq * j;
-#pragma unroll
-                    for (int t = 0; t < Bq; ++t) u[j][t] = S[kk * C::RowStride + t];
-                    dft<Bq, -1>(u[j]);
-                }
-#pragma unroll
-                for (int j = 0; j < J; ++j) {
-                    const int kk = n1 + Bq * j;
-#pragma unroll
-                    for (int k1 = 0; k1 < Bq; ++k1) {
-                        const int k = 16 * k1 + kk;
-                        if (k < m2 || k > W - m2) Zs[k] = u[j][k1];
-                    }
-                }
-            }
-            __syncwarp();
-            if (active) {
-                for (int k = n1; k < m2; k += Bq) {
-                    const float2 zk = Zs[k], zm = Zs[(W - k) & (W - 1)];
-                    Y[qa * ys + k] = make_float2(0.5f * (zk.x + zm.x), 0.5f * (zk.y - zm.y));
-                    Y[(qa + 1) * ys + k] = make_float2(0.5f * (zk.y + zm.y), -0.5f * (zk.x - zm.x));
-                }
-            }
-            __syncwarp();
+            const float* ra = xp + (size_t)(p + P * qa) * W;
+            row_pair_forward<W>(ra, ra + (size_t)P * W, S, Y + qa * ys, Y + (qa + 1) * ys, t, m2,
+                                tw_w, active);
         }
     }
     __syncthreads();
 
     // ---- columns --------------------------------------------------------
-    {
-        constexpr int Bq = C::BqR;
-        constexpr int J = 16 / Bq;
-        constexpr int CP = C::ColsPerPass;
-        const int cs = threadIdx.x % CP;   // column within the pass
-        const int n1 = threadIdx.x / CP;   // position within the column transform
-        float2* S = scr + cs * C::ColScr;  // S[kk][n1] with row stride Bq
-        const int R2 = 2 * m1;
-        const size_t xbase = (size_t)plane * R2 * m2;
-        for (int c0 = 0; c0 < m2; c0 += CP) {
-            const int col = c0 + cs;
-            const bool active = col < m2;
-            if (active) {
-                float2 v[16];
-#pragma unroll
-                for (int n2 = 0; n2 < 16; ++n2) v[n2] = Y[(n1 + Bq * n2) * ys + col];
-                dft<16, -1>(v);
-#pragma unroll
-                for (int kk = 1; kk < 16; ++kk) v[kk] = cmul(v[kk], root<-1>(tw_h, n1 * kk * P, H));
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) S[kk * Bq + n1] = v[kk];
-            }
-            __syncthreads();
-            if (active) {
-#pragma unroll
-                for (int j = 0; j < J; ++j) {
-                    const int kk = n1 + Bq * j;
-                    float2 u[Bq];
-#pragma unroll
-                    for (int t = 0; t < Bq; ++t) u[t] = S[kk * Bq + t];
-                    dft<Bq, -1>(u);
-#pragma unroll
-                    for (int k1 = 0; k1 < Bq; ++k1) {
-                        int kf;
-                        const int r = row_of_residue(16 * k1 + kk, R, H, m1, &kf);
-                        if (r < 0) continue;
-                        float2 val = cscale(u[k1], scale);
-                        float2* dst = X + xbase + (size_t)r * m2 + col;
-                        if (P == 1) {
-                            *dst = val;
-                        } else {
-                            val = cmul(val, root<-1>(tw_h, kf * p, H));
-                            atomicAdd(&dst->x, val.x);
-                            atomicAdd(&dst->y, val.y);
-                        }
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
+    columns_forward<R>(scr, Y, ys, X, (size_t)plane * 2 * m1 * m2, H, m1, m2, P, p, scale, tw_h);
 }
 
 // ---------------------------------------------------------------- inverse ---
 template <int W, int R>
-__global__ void __launch_bounds__(kFT)
+__global__ void __launch_bounds__(kFT, (FusedCfg<W, R>::MinBlocks))
 inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m1, int m2,
                  int P, float scale, const float2* __restrict__ tw_w,
                  const float2* __restrict__ tw_h) {
@@ -208,122 +316,24 @@ inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int
     const float2* Zp = Z + (size_t)plane * R2 * m2;
 
     // ---- columns: retained rows of Z -> V[q][col], q in [0, R) ----------
-    {
-        constexpr int Bq = C::BqR;
-        constexpr int J = 16 / Bq;
-        constexpr int CP = C::ColsPerPass;
-        const int cs = threadIdx.x % CP;
-        const int t = threadIdx.x / CP;
-        float2* S = scr + cs * C::ColScr;  // S[n1][kk] with row stride 16
-        for (int c0 = 0; c0 < m2; c0 += CP) {
-            const int col = c0 + cs;
-            const bool active = col < m2;
-            if (active) {
-                // pass 1 (transposed): for kk = t + Bq*j, inverse Bq-point DFT over
-                // k1 of U[16*k1 + kk], then times e^{+2 pi i n1 kk / R}
-#pragma unroll
-                for (int j = 0; j < J; ++j) {
-                    const int kk = t + Bq * j;
-                    float2 u[Bq];
-#pragma unroll
-                    for (int k1 = 0; k1 < Bq; ++k1) {
-                        int kf;
-                        const int r = row_of_residue(16 * k1 + kk, R, H, m1, &kf);
-                        float2 val = make_float2(0.f, 0.f);
-                        if (r >= 0) {
-                            val = __ldg(&Zp[(size_t)r * m2 + col]);
-                            if (P > 1) val = cmul(val, root<1>(tw_h, kf * p, H));
-                        }
-                        u[k1] = val;
-                    }
-                    dft<Bq, 1>(u);
-#pragma unroll
-                    for (int n1 = 0; n1 < Bq; ++n1) {
-                        const float2 w = n1 == 0 ? u[n1] : cmul(u[n1], root<1>(tw_h, n1 * kk * P, H));
-                        S[n1 * 16 + kk] = w;
-                    }
-                }
-            }
-            __syncthreads();
-            if (active) {
-                // pass 2: thread n1 = t, inverse 16-point DFT over kk
-                const int n1 = t;
-                float2 v[16];
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) v[kk] = S[n1 * 16 + kk];
-                dft<16, 1>(v);
-#pragma unroll
-                for (int n2 = 0; n2 < 16; ++n2) V[(n1 + Bq * n2) * ys + col] = v[n2];
-            }
-            __syncthreads();
-        }
-    }
+    columns_inverse<R>(scr, V, ys, Zp, H, m1, m2, P, p, tw_h);
+    __syncthreads();
 
     // ---- rows: pairs of V rows -> two real output rows ------------------
     {
         constexpr int Bq = C::BqW;
-        constexpr int J = 16 / Bq;
         const int g = threadIdx.x / Bq, t = threadIdx.x % Bq;
-        float2* S = scr + g * C::RowScr;  // S[n1][kk] with row stride 17
+        float2* S = scr + g * C::RowScr;
         float* yp = y + (size_t)plane * H * W;
         constexpr int npairs = R / 2;
         constexpr int iters = (npairs + C::RowGroups - 1) / C::RowGroups;
-        const int half = W / 2;
         for (int it = 0; it < iters; ++it) {
             const int pair = g + it * C::RowGroups;
             const bool active = pair < npairs;
             const int qa = 2 * pair;
-            if (active) {
-                const float2* Va = V + qa * ys;
-                const float2* Vb = Va + ys;
-#pragma unroll
-                for (int j = 0; j < J; ++j) {
-                    const int kk = t + Bq * j;
-                    float2 u[Bq];
-#pragma unroll
-                    for (int k1 = 0; k1 < Bq; ++k1) {
-                        const int k = 16 * k1 + kk;  // bin of the packed spectrum U
-                        float2 val = make_float2(0.f, 0.f);
-                        if (k == 0 || k == half) {
-                            if (k < m2) val = make_float2(Va[k].x, Vb[k].x);
-                        } else if (k < half) {
-                            if (k < m2) {
-                                const float2 a = Va[k], b = Vb[k];
-                                val = make_float2(a.x - b.y, a.y + b.x);
-                            }
-                        } else {
-                            const int kr = W - k;
-                            if (kr < m2) {
-                                const float2 a = Va[kr], b = Vb[kr];
-                                val = make_float2(a.x + b.y, b.x - a.y);
-                            }
-                        }
-                        u[k1] = val;
-                    }
-                    dft<Bq, 1>(u);
-#pragma unroll
-                    for (int n1 = 0; n1 < Bq; ++n1) {
-                        const float2 w = n1 == 0 ? u[n1] : cmul(u[n1], root<1>(tw_w, n1 * kk, W));
-                        S[n1 * 17 + kk] = w;
-                    }
-                }
-            }
-            __syncwarp();
-            if (active) {
-                const int n1 = t;
-                float2 v[16];
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) v[kk] = S[n1 * 17 + kk];
-                dft<16, 1>(v);
-                float* ya = yp + (size_t)(p + P * qa) * W;
-                float* yb = yp + (size_t)(p + P * (qa + 1)) * W;
-#pragma unroll
-                for (int n2 = 0; n2 < 16; ++n2) {
-                    ya[n1 + Bq * n2] = v[n2].x * scale;
-                    yb[n1 + Bq * n2] = v[n2].y * scale;
-                }
-            }
-            __syncwarp();
+            float* ya = yp + (size_t)(p + P * qa) * W;
+            row_pair_inverse<W>(V + qa * ys, V + (qa + 1) * ys, S, ya, ya + (size_t)P * W, t, m2,
+                                tw_w, scale, active);
         }
     }
 }
@@ -412,7 +422,8 @@ cudaError_t stages_fused_init() {
 size_t fused_smem_bytes_any(int W, int R, int m2);
 
 bool fused_supported(int W, int H, int m1, int m2, int* R_out) {
-    if (W < 32 || W > 256 || H < 32) return false;
+    if (W < 32 || H < 32) return false;
+    if (W > 256 && m2 > 64) return false;  // long rows keep at most 64 columns
     // the column length R: the whole column when it fits, else the smallest
     // power of two >= max(2*m1, 32) that divides H, at most 256
     int R = H <= 256 ? H : 0;
@@ -422,7 +433,8 @@ bool fused_supported(int W, int H, int m1, int m2, int* R_out) {
         if (R > 256) return false;
     }
     if (R < 2 * m1 || R > H) return false;
-    if (fused_smem_bytes_any(W, R, m2) > 227 * 1024) return false;
+    const size_t smem = W <= 256 ? fused_smem_bytes_any(W, R, m2) : big_smem_bytes_any(W, R, m2);
+    if (smem > 227 * 1024) return false;
     *R_out = R;
     return true;
 }
@@ -450,14 +462,15 @@ cudaError_t launch_forward_fused(const fno_plan_s& p, const float* x, float2* X,
         if (e == cudaSuccess && ctx) e = ctx->mark(s);
         if (e != cudaSuccess) return e;
     }
-    e = dispatch<true>(p, x, X, nullptr, nullptr, s);
+    e = p.W <= 256 ? dispatch<true>(p, x, X, nullptr, nullptr, s) : launch_forward_big(p, x, X, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
 
 cudaError_t launch_inverse_fused(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s,
                                  fno_launch_ctx* ctx) {
-    cudaError_t e = dispatch<false>(p, nullptr, nullptr, Z, y, s);
+    cudaError_t e = p.W <= 256 ? dispatch<false>(p, nullptr, nullptr, Z, y, s)
+                               : launch_inverse_big(p, Z, y, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }

@@ -33,6 +33,12 @@ EDGE_SHAPES = [
     (3, 33, 40, 32, 32, 3, 5),      # B < batch tile, Cin % IC != 0, Cout % 32 != 0, NM % 4 == 2
     (5, 16, 96, 64, 32, 4, 4),      # B = 5 -> batch tile 8 split over two warp groups
     (20, 32, 32, 32, 32, 2, 3),     # B > 16: two batch tiles
+    # long rows (three-level row transform, shuffle reduce-scatter)
+    (2, 3, 4, 64, 512, 16, 33),     # W = 512
+    (1, 2, 2, 32, 1024, 8, 64),     # W = 1024, the largest supported m2
+    (1, 1, 2, 256, 4096, 32, 17),   # W = 4096, one row group per CTA
+    (2, 2, 3, 512, 2048, 128, 5),   # 2*m1 = 256 -> R = 256, P = 2
+    (1, 3, 3, 1024, 2048, 64, 1),   # a single kept column
 ]
 
 
