@@ -92,6 +92,11 @@ void set_kernel(fno_plan_s* p, int k, const char* name, size_t bytes, size_t flo
     p->kernels[k].flops = flops;
 }
 
+const char* mix_name(const fno_plan_s* p) {
+    if (p->mix_path == 2) return p->tc_split == 3 ? "mix_tc_3xtf32" : "mix_tc_tf32";
+    return p->mix_path == 1 ? "mix_tma" : "mix_fma";
+}
+
 double fft_flops(double L) { return 5.0 * L * std::log2(L); }
 
 // Kernel list of the shape-generic path (stages_generic.cu + mix_fma.cu).
@@ -100,7 +105,7 @@ void describe_generic(fno_plan_s* p) {
     const size_t Ti = 8ull * Pi * p->H * p->m2, To = 8ull * Po * p->H * p->m2;
     set_kernel(p, 0, "fwd_rows", x_bytes(p) + Ti, (size_t)(fft_flops(p->W) * Pi * p->H / 2));
     set_kernel(p, 1, "fwd_cols", Ti + X_bytes(p), (size_t)(fft_flops(p->H) * Pi * p->m2));
-    set_kernel(p, 2, p->mix_path == 1 ? "mix_tma" : "mix_fma", X_bytes(p) + w_bytes(p) + Z_bytes(p),
+    set_kernel(p, 2, mix_name(p), X_bytes(p) + w_bytes(p) + Z_bytes(p),
                8ull * p->B * p->Cin * p->Cout * p->nm);
     set_kernel(p, 3, "inv_cols", Z_bytes(p) + To, (size_t)(fft_flops(p->H) * Po * p->m2));
     set_kernel(p, 4, "inv_rows", To + y_bytes(p), (size_t)(fft_flops(p->W) * Po * p->H / 2));
@@ -115,7 +120,7 @@ void describe_fused(fno_plan_s* p) {
     const double fl_f = Pi * (fft_flops(p->W) * p->H / 2 + fft_flops(p->R) * p->m2 * p->P);
     const double fl_i = Po * (fft_flops(p->W) * p->H / 2 + fft_flops(p->R) * p->m2 * p->P);
     set_kernel(p, k++, "fwd_fused", x_bytes(p) + X_bytes(p), (size_t)fl_f);
-    set_kernel(p, k++, p->mix_path == 1 ? "mix_tma" : "mix_fma", X_bytes(p) + w_bytes(p) + Z_bytes(p),
+    set_kernel(p, k++, mix_name(p), X_bytes(p) + w_bytes(p) + Z_bytes(p),
                8ull * p->B * p->Cin * p->Cout * p->nm);
     set_kernel(p, k++, "inv_fused", Z_bytes(p) + y_bytes(p), (size_t)fl_i);
     p->launches = k;
@@ -133,8 +138,10 @@ cudaError_t run_inverse(const fno_plan_s& p, const float2* Z, float* y, float2* 
 
 cudaError_t run_mix(const fno_plan_s& p, const float2* X, const float2* w, float2* Z, cudaStream_t s,
                     fno_launch_ctx* ctx) {
+    if (p.mix_path == 2) return launch_mix_tc(p, X, w, Z, p.tc_split, s, ctx);
     return p.mix_path == 1 ? launch_mix_tma(p, X, w, Z, s, ctx) : launch_mix_modes(p, X, w, Z, s, ctx);
 }
+
 
 fno_status_t cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return FNO_OK;
@@ -169,7 +176,6 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     if (st != FNO_OK) return st;
     if (prec != FNO_PREC_FP32 && prec != FNO_PREC_TF32 && prec != FNO_PREC_3XTF32)
         return FNO_ERR_INVALID_ARG;
-    if (prec != FNO_PREC_FP32) return FNO_ERR_UNSUPPORTED;
 
     std::call_once(g_init_once, [] {
         g_init_err = stages_generic_init();
@@ -177,6 +183,7 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
         if (g_init_err == cudaSuccess) g_init_err = stages_big_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_tma_init();
+        if (g_init_err == cudaSuccess) g_init_err = mix_tc_init();
     });
     if (g_init_err != cudaSuccess) return FNO_ERR_CUDA;
 
@@ -193,6 +200,11 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     p->R = p->path == 1 ? R : H;
     p->P = H / p->R;
     p->mix_path = mix_tma_supported(B, Cin, Cout, p->nm) ? 1 : 0;
+    p->tc_split = prec == FNO_PREC_3XTF32 ? 3 : 1;
+    // tensor cores for the contraction only where it is a real dense product
+    if (prec != FNO_PREC_FP32 && Cin >= 32 && Cout >= 32 &&
+        mix_tc_supported(B, Cin, Cout, p->nm, p->tc_split))
+        p->mix_path = 2;
 
     // workspace: X | Z | T (T only on the shape-generic path)
     size_t off = 0;
@@ -207,13 +219,13 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     if (p->path == 1) {
         describe_fused(p);
         std::snprintf(p->desc, sizeof(p->desc),
-                      "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|%s|inv-cols+rows, fp32", W, p->R,
-                      p->P, p->mix_path == 1 ? "mix-tma" : "mix-fma");
+                      "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|%s|inv-cols+rows", W, p->R,
+                      p->P, mix_name(p));
     } else {
         describe_generic(p);
         std::snprintf(p->desc, sizeof(p->desc),
-                      "generic: rows-fft(W=%d)|cols-fft(H=%d)|%s|icols-fft|irows-fft, fp32", W, H,
-                      p->mix_path == 1 ? "mix-tma" : "mix-fma");
+                      "generic: rows-fft(W=%d)|cols-fft(H=%d)|%s|icols-fft|irows-fft", W, H,
+                      mix_name(p));
     }
 
     std::vector<float2> th = twiddles(H), tw = twiddles(W);

@@ -45,7 +45,8 @@ struct fno_plan_s {
     // workspace layout (byte offsets, each 256-byte aligned)
     size_t off_X, off_Z, off_T, ws_bytes;
     int path;               // 0: shape-generic kernels, 1: fused transform kernels
-    int mix_path;           // 0: mix_fma (shared-memory tiles), 1: mix_tma (TMA-fed)
+    int mix_path;           // 0: mix_fma, 1: mix_tma (TMA-fed fp32), 2: mix_tc (tcgen05)
+    int tc_split;           // mix_tc: 1 (TF32) or 3 (split TF32, hi*hi + hi*lo + lo*hi)
     int R, P;               // fused path: column length per CTA and H / R
     int launches;           // kernel launches per execute
     fno_kernel_desc kernels[kMaxKernels];
@@ -77,6 +78,12 @@ cudaError_t mix_tma_init();
 bool mix_tma_supported(int B, int Cin, int Cout, int nm);
 cudaError_t launch_mix_tma(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                            cudaStream_t s, fno_launch_ctx* ctx);
+
+// tcgen05 tensor-core contraction (mix_tc.cu).
+cudaError_t mix_tc_init();
+bool mix_tc_supported(int B, int Cin, int Cout, int nm, int split);
+cudaError_t launch_mix_tc(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
+                          int split, cudaStream_t s, fno_launch_ctx* ctx);
 
 // Stage launchers (all asynchronous on stream s).
 // Each launcher calls ctx->mark(s) after every kernel it enqueues.

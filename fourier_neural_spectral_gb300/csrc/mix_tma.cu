@@ -180,154 +180,6 @@ mix_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     }
 }
 
-// ---------------------------------------------------------------------------
-// Register-tiled variant.  Each thread accumulates 4 output channels x BC
-// batch rows x 2 modes (8*BC complex accumulators), so every shared-memory
-// load feeds 8 or more FMAs.  A warp covers 8 channel groups x 4 batch groups
-// (or fewer batch groups when the batch is small): lanes with the same
-// channel group read the same w words and lanes with the same batch group the
-// same X words, which the hardware broadcasts.  Lanes are laid out as
-// (channel-group low bits: 4) x (mode half: 2) x (batch group) and each lane
-// walks its 4 channel rows starting at row (k + og) mod 4, so at every step
-// the 8 distinct 16-byte w chunks a warp reads lie in 8 different bank groups.
-struct MixTileCfg {
-    int OC, IC, BT, BC, NBG, threads;
-    size_t w_bytes, x_off, stage, smem;
-};
-
-__host__ __device__ inline size_t round1024(size_t v) { return (v + 1023) / 1024 * 1024; }
-
-MixTileCfg mix_tile_cfg(int B, int Cin, int Cout) {
-    MixTileCfg c;
-    c.OC = std::min(128, (Cout + 31) / 32 * 32);
-    int bt = 1;
-    while (bt < B && bt < 16) bt <<= 1;
-    c.BT = bt;
-    c.BC = std::min(bt, 4);
-    c.NBG = bt / c.BC;
-    c.threads = (c.OC / 4) * c.NBG * 2;
-    c.IC = std::max(1, std::min(Cin, 8192 / (32 * c.OC)));
-    c.w_bytes = (size_t)32 * c.OC * c.IC;
-    c.x_off = round1024(c.w_bytes);
-    c.stage = c.x_off + round1024((size_t)32 * c.IC * c.BT);
-    c.smem = 1024 + 1024 + (size_t)kStages * c.stage;  // barriers + alignment slack + ring
-    return c;
-}
-
-template <int BC>
-__global__ void __launch_bounds__(256)
-mix_tile_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                float2* __restrict__ Z, int B, int Cin, int Cout, int NM, int OC, int IC, int BT,
-                int NBG, unsigned* __restrict__ err) {
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
-    // ring start aligned to 1 KB (the swizzle atom)
-    unsigned char* ring = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1024 + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x;
-    // thread -> (channel group og, batch group bg, mode half mh)
-    const int og_lo = tid & 3, mh = (tid >> 2) & 1, rest = tid >> 3;
-    const int bg = rest % NBG, og = og_lo + 4 * (rest / NBG);
-    const int m0 = blockIdx.x * 4, o0 = blockIdx.y * OC, b0 = blockIdx.z * BT;
-    const int nch = (Cin + IC - 1) / IC;
-    const uint32_t w_bytes = 32u * OC * IC;
-    const uint32_t x_off = (w_bytes + 1023u) & ~1023u;
-    const uint32_t x_bytes = 32u * IC * BT;
-    const uint32_t stage = x_off + ((x_bytes + 1023u) & ~1023u);
-    const uint32_t tx = w_bytes + x_bytes;
-
-    if (tid == 0) {
-        prefetch_tensormap(&tmW);
-        prefetch_tensormap(&tmX);
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-    int issued = 0;
-    if (tid == 0) {
-        for (; issued < kStages && issued < nch; ++issued) {
-            unsigned char* st = ring + (size_t)issued * stage;
-            mbar_arrive_expect_tx(&bars[issued], tx);
-            tma_load_3d(st, &tmW, 2 * m0, o0, issued * IC, &bars[issued]);
-            tma_load_3d(st + x_off, &tmX, 2 * m0, issued * IC, b0, &bars[issued]);
-        }
-    }
-
-    float2 acc[4][BC][2];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int bb = 0; bb < BC; ++bb) acc[j][bb][0] = acc[j][bb][1] = make_float2(0.f, 0.f);
-
-    int consumed = 0;
-    bool timed_out = false;
-    for (int c = 0; c < nch; ++c) {
-        const int s = c % kStages;
-        const bool ok = wait_parity_bounded(&bars[s], (uint32_t)((c / kStages) & 1), err);
-        if (__syncthreads_or(!ok)) {
-            timed_out = true;
-            break;
-        }
-        consumed = c + 1;
-        const unsigned char* st = ring + (size_t)s * stage;
-        const int ni = min(IC, Cin - c * IC);
-        for (int ii = 0; ii < ni; ++ii) {
-            float4 w[4], xv[BC];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {  // w[k] is channel row (k + og) mod 4
-                const uint32_t off = (uint32_t)((ii * OC + og * 4 + ((k + og_lo) & 3)) * 32 + 16 * mh);
-                w[k] = *reinterpret_cast<const float4*>(st + off);
-            }
-#pragma unroll
-            for (int bb = 0; bb < BC; ++bb) {
-                const uint32_t off = (uint32_t)(((bg * BC + bb) * IC + ii) * 32 + 16 * mh);
-                xv[bb] = *reinterpret_cast<const float4*>(st + x_off + off);
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int bb = 0; bb < BC; ++bb) {
-                    cmac(acc[j][bb][0], make_float2(xv[bb].x, xv[bb].y), make_float2(w[j].x, w[j].y));
-                    cmac(acc[j][bb][1], make_float2(xv[bb].z, xv[bb].w), make_float2(w[j].z, w[j].w));
-                }
-        }
-        __syncthreads();
-        if (tid == 0 && issued < nch) {
-            unsigned char* st2 = ring + (size_t)s * stage;
-            mbar_arrive_expect_tx(&bars[s], tx);
-            tma_load_3d(st2, &tmW, 2 * m0, o0, issued * IC, &bars[s]);
-            tma_load_3d(st2 + x_off, &tmX, 2 * m0, issued * IC, b0, &bars[s]);
-            ++issued;
-        }
-    }
-    if (timed_out) {
-        if (tid == 0)
-            for (int c = consumed; c < issued; ++c)
-                wait_parity_bounded(&bars[c % kStages], (uint32_t)((c / kStages) & 1), err);
-        __syncthreads();
-        return;
-    }
-    const int m = m0 + 2 * mh;
-    if (m >= NM) return;
-    const bool pair = m + 1 < NM;  // NM is even, so this always holds; kept for safety
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int o = o0 + og * 4 + ((j + og_lo) & 3);
-        if (o >= Cout) continue;
-#pragma unroll
-        for (int bb = 0; bb < BC; ++bb) {
-            const int b = b0 + bg * BC + bb;
-            if (b >= B) break;
-            float2* zp = Z + ((size_t)b * Cout + o) * NM + m;
-            if (pair)
-                *reinterpret_cast<float4*>(zp) =
-                    make_float4(acc[j][bb][0].x, acc[j][bb][0].y, acc[j][bb][1].x, acc[j][bb][1].y);
-            else
-                zp[0] = acc[j][bb][0];
-        }
-    }
-}
-
 template <int BTT>
 cudaError_t launch_btt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, int B, int Cin,
                        int Cout, int NM, const MixTmaCfg& c, unsigned* err, cudaStream_t s) {
@@ -340,12 +192,6 @@ cudaError_t launch_btt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, 
         mix_tma_kernel<BTT, 1><<<grid, threads, c.smem, s>>>(mw, mx, Z, B, Cin, Cout, NM, c.OC,
                                                              c.IC, c.BT, err);
     return cudaGetLastError();
-}
-
-template <int BC>
-cudaError_t set_attr_tile() {
-    return cudaFuncSetAttribute(mix_tile_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                227 * 1024);
 }
 
 template <int BTT>
@@ -381,9 +227,6 @@ cudaError_t mix_tma_init() {
     if (e == cudaSuccess) e = set_attr<2>();
     if (e == cudaSuccess) e = set_attr<4>();
     if (e == cudaSuccess) e = set_attr<8>();
-    if (e == cudaSuccess) e = set_attr_tile<1>();
-    if (e == cudaSuccess) e = set_attr_tile<2>();
-    if (e == cudaSuccess) e = set_attr_tile<4>();
     if (e == cudaSuccess && !fno_get_encode_tiled()) e = cudaErrorNotSupported;
     return e;
 }
@@ -397,8 +240,7 @@ bool mix_tma_supported(int B, int Cin, int Cout, int nm) {
 // dims (2*NM, d1, d2), box (8 floats = 4 modes, b1, b2).  Out-of-range box
 // elements are filled with zeros.
 static bool encode_modes_map(CUtensorMap* map, const float2* base, int NM, int d1, int d2,
-                             int b1, int b2,
-                             CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
+                             int b1, int b2) {
     fno_encode_tiled_fn enc = fno_get_encode_tiled();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)NM * 2, (cuuint64_t)d1, (cuuint64_t)d2};
@@ -406,34 +248,13 @@ static bool encode_modes_map(CUtensorMap* map, const float2* base, int NM, int d
     cuuint32_t box[3] = {8, (cuuint32_t)b1, (cuuint32_t)b2};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float2*>(base), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-static bool use_tile(int B, int Cin, int Cout) {
-    const MixTileCfg t = mix_tile_cfg(B, Cin, Cout);
-    return t.threads >= 64 && t.smem <= 227 * 1024;
-}
-
 cudaError_t launch_mix_tma(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                            cudaStream_t s, fno_launch_ctx* ctx) {
-    if (use_tile(p.B, p.Cin, p.Cout)) {
-        const MixTileCfg t = mix_tile_cfg(p.B, p.Cin, p.Cout);
-        CUtensorMap mw, mx;
-        if (!encode_modes_map(&mw, w, p.nm, p.Cout, p.Cin, t.OC, t.IC) ||
-            !encode_modes_map(&mx, X, p.nm, p.Cin, p.B, t.IC, t.BT))
-            return cudaErrorInvalidValue;
-        dim3 grid((p.nm + 3) / 4, (p.Cout + t.OC - 1) / t.OC, (p.B + t.BT - 1) / t.BT);
-        switch (t.BC) {
-            case 1: mix_tile_kernel<1><<<grid, t.threads, t.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, t.OC, t.IC, t.BT, t.NBG, p.err); break;
-            case 2: mix_tile_kernel<2><<<grid, t.threads, t.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, t.OC, t.IC, t.BT, t.NBG, p.err); break;
-            default: mix_tile_kernel<4><<<grid, t.threads, t.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, t.OC, t.IC, t.BT, t.NBG, p.err); break;
-        }
-        cudaError_t e = cudaGetLastError();
-        if (e == cudaSuccess && ctx) e = ctx->mark(s);
-        return e;
-    }
     const MixTmaCfg c = mix_tma_cfg(p.B, p.Cin, p.Cout);
     CUtensorMap mw, mx;
     if (!encode_modes_map(&mw, w, p.nm, p.Cout, p.Cin, c.OC, c.IC) ||

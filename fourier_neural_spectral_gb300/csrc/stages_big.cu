@@ -25,11 +25,13 @@
 #include "fft_reg.cuh"
 #include "fused_columns.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace fno {
 namespace {
 
 constexpr int kBT = 256;      // threads per CTA
+constexpr int kPrefetch = 4;  // row pairs a group asks L2 to fetch ahead of use
 constexpr int kNL = 4;        // candidate k1 per side: ceil(m2 / 16) <= 4, i.e. m2 <= 64
 
 template <int W>
@@ -124,10 +126,21 @@ fwd_big_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m
 
     constexpr int npairs = R / 2;
     constexpr int iters = (npairs + B::Groups - 1) / B::Groups;
+    // rows of pair j of this group: p + P*(2j) and p + P*(2j + 1)
+    auto prefetch_pair = [&](int pr) {
+        if (pr < npairs) {
+            const float* r0 = xp + (size_t)(p + P * 2 * pr) * W;
+            prefetch_l2_bulk(r0, W * sizeof(float));
+            prefetch_l2_bulk(r0 + (size_t)P * W, W * sizeof(float));
+        }
+    };
+    if (t == 0)
+        for (int d = 1; d <= kPrefetch; ++d) prefetch_pair(g + d * B::Groups);
     for (int it = 0; it < iters; ++it) {
         const int pair = g + it * B::Groups;
         const bool active = pair < npairs;  // uniform over the group
         const int qa = 2 * pair;
+        if (t == 0) prefetch_pair(pair + (kPrefetch + 1) * B::Groups);
         if (active) {
             const float* ra = xp + (size_t)(p + P * qa) * W;
             const float* rb = ra + (size_t)P * W;

@@ -1,0 +1,79 @@
+"""The tcgen05 tensor-core contraction (precision "tf32" and "3xtf32") against
+the oracle: stage a3 alone on seeded spectra, and the whole layer."""
+import numpy as np
+import pytest
+
+import oracle
+from fourier_neural_spectral_gb300 import synth
+
+from gpu_helpers import TF32_REL_L2, errors, f32pairs_to_cplx, run_layer, to_dev
+
+pytestmark = pytest.mark.gpu
+
+# tolerance of the split-TF32 path: fp32-level (the fp32 path's bound)
+SPLIT_REL_L2 = 1e-5
+
+MIX_SHAPES = [
+    # B, Cin, Cout, m1, m2
+    (1, 32, 32, 1, 2),      # one CTA: 4 modes, padded batch and channel block
+    (16, 64, 64, 4, 4),     # the 128x128 workload's channel/batch shape
+    (4, 128, 128, 2, 4),    # two channel blocks, batch padded 4 -> 8
+    (3, 40, 100, 3, 2),     # ragged Cin (last chunk partial) and Cout (partial block)
+    (32, 64, 64, 1, 2),     # largest batch handled
+]
+
+
+def mix_case(B, Cin, Cout, m1, m2, precision):
+    import torch
+    from fourier_neural_spectral_gb300 import fnospec
+    H = 2
+    while H < 2 * m1:
+        H *= 2
+    W = 2
+    while W // 2 + 1 < m2:
+        W *= 2
+    plan = fnospec.Plan(B, Cin, Cout, H, W, m1, m2, precision)
+    X = synth.normal_f32((B, Cin, 2 * m1, m2, 2), seed=21, stream=7)
+    w = synth.uniform_f32((Cin, Cout, 2 * m1, m2, 2), scale=1.0 / (Cin * Cout), seed=21, stream=8)
+    Zt = torch.empty((B, Cout, 2 * m1, m2, 2), dtype=torch.float32, device="cuda")
+    plan.fno_mix_modes(to_dev(X), to_dev(w), Zt)
+    torch.cuda.synchronize()
+    assert plan.fno_get_device_status() == fnospec.FNO_OK
+    ref = oracle.mix_modes(f32pairs_to_cplx(X), f32pairs_to_cplx(w))
+    return errors(f32pairs_to_cplx(Zt.cpu().numpy()), ref), plan
+
+
+@pytest.mark.parametrize("shape", MIX_SHAPES)
+def test_tc_mix_stage_tf32(cuda_lib, shape):
+    (rel, mx), plan = mix_case(*shape, "tf32")
+    assert "mix_tc_tf32" in plan.description, plan.description
+    assert rel <= TF32_REL_L2, rel
+
+
+@pytest.mark.parametrize("shape", MIX_SHAPES)
+def test_tc_mix_stage_split_tf32(cuda_lib, shape):
+    (rel, mx), plan = mix_case(*shape, "3xtf32")
+    assert "mix_tc_3xtf32" in plan.description, plan.description
+    assert rel <= SPLIT_REL_L2, rel
+
+
+@pytest.mark.parametrize("name", ["B8_C32_64x64_m16_smooth", "B16_C64_128x128_m32",
+                                  "B4_C128_256x256_m64"])
+@pytest.mark.parametrize("precision", ["tf32", "3xtf32"])
+def test_tc_layer_matches_oracle(cuda_lib, name, precision):
+    from test_gpu_parity import oracle_layer_threaded
+    cfg = synth.CONFIGS[name]
+    x, w = synth.make_inputs(cfg)
+    y, plan = run_layer(x, w, cfg.m1, cfg.m2, precision)
+    assert "mix_tc" in plan.description
+    ref = oracle_layer_threaded(cfg, x, w)
+    rel, mx = errors(y, ref)
+    bound = TF32_REL_L2 if precision == "tf32" else SPLIT_REL_L2
+    print(f"{name} {precision}: rel-L2 {rel:.2e} max-abs {mx:.2e}")
+    assert rel <= bound, rel
+
+
+def test_small_channels_use_fma_even_in_tc_mode(cuda_lib):
+    from fourier_neural_spectral_gb300 import fnospec
+    plan = fnospec.Plan(2, 4, 4, 16, 16, 4, 4, "tf32")
+    assert "mix_tc" not in plan.description
