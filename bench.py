@@ -135,6 +135,29 @@ def barrier(world: int):
         dist.barrier()
 
 
+def aggregate_value(world: int, batch: int, steps: int, elapsed_ms_max: float) -> float:
+    """Whole-job samples/s: every rank runs its own replica of the workload
+    (weak scaling), timed by the slowest rank."""
+    return world * batch * steps / (elapsed_ms_max / 1e3)
+
+
+def measured_traffic(workload: str, kernel: str, precision: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload`, from the
+    ncu summary table in profiles/dram_traffic.md, or None if not captured for
+    the current version of that kernel."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    try:
+        with open(path) as f:
+            for line in f:
+                cells = [c.strip() for c in line.strip().strip("|").split("|")]
+                if len(cells) >= 5 and cells[0] == workload and cells[1] == kernel and \
+                        cells[2] == precision:
+                    return float(cells[3]) + float(cells[4])
+    except OSError:
+        pass
+    return None
+
+
 # ---------------------------------------------------------- oracle (host) ---
 
 def oracle_sample_batch(cfg, budget: float = 2.5e9) -> int:
@@ -280,7 +303,7 @@ def run_ours(args, cfg):
     per_step = [evs[0].elapsed_time(evs[-1]) for evs in evsets]
     per_kernel = [[evs[k].elapsed_time(evs[k + 1]) for evs in evsets] for k in range(nk)]
     ms_per_step = elapsed_ms / args.steps
-    value = world * cfg.B * args.steps / (elapsed_ms / 1e3)
+    value = aggregate_value(world, cfg.B, args.steps, elapsed_ms)
 
     # dominant kernel and its roofline
     kmean = [statistics.mean(v) for v in per_kernel]
@@ -289,8 +312,9 @@ def run_ours(args, cfg):
     hbm = float(peaks["hbm_gbs"])
     k_gbs = kinfo["bytes"] / (kmean[kdom] * 1e-3) / 1e9
     k_flops = kinfo["flops"] / (kmean[kdom] * 1e-3) / 1e12
+    traffic = measured_traffic(cfg.name, kinfo["name"], args.precision)
     roofline = {"kernel": kinfo["name"], "bound": "hbm", "achieved": k_gbs, "peak": hbm,
-                "unit": "GB/s", "frac": k_gbs / hbm, "traffic": None,
+                "unit": "GB/s", "frac": k_gbs / hbm, "traffic": traffic,
                 "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy)",
                 "bytes_per_launch": kinfo["bytes"], "ms_per_launch": kmean[kdom],
                 "achieved_tflops": k_flops}
@@ -334,7 +358,7 @@ def run_ours(args, cfg):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    e2e_value = world * cfg.B * e2e_steps / (e2e_ms / 1e3)
+    e2e_value = aggregate_value(world, cfg.B, e2e_steps, e2e_ms)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -25,11 +25,20 @@ struct ColCfg {
     static constexpr int Scratch = CP * Scr;
 };
 
-template <int R>
+// Whether output residue block k1 (residues 16*k1 .. 16*k1 + 15) can hold a
+// retained frequency when m1 is the compile-time constant M1S (> 0); always
+// true when M1S = 0 (m1 known only at run time).
+template <int R, int M1S>
+__device__ __forceinline__ constexpr bool k1_live(int k1) {
+    return M1S == 0 || 16 * k1 < M1S || 16 * k1 + 15 >= R - M1S;
+}
+
+template <int R, int M1S = 0>
 __device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, int ys,
                                                 float2* __restrict__ X, size_t xbase, int H,
                                                 int m1, int m2, int P, int p, float scale,
                                                 const float2* __restrict__ tw_h) {
+    if (M1S) m1 = M1S;
     constexpr int Bq = ColCfg<R>::Bq;
     constexpr int J = 16 / Bq;
     constexpr int CP = ColCfg<R>::CP;
@@ -60,6 +69,7 @@ __device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, in
                 dft<Bq, -1>(u);
 #pragma unroll
                 for (int k1 = 0; k1 < Bq; ++k1) {
+                    if (!k1_live<R, M1S>(k1)) continue;
                     int kf;
                     const int r = row_of_residue(16 * k1 + kk, R, H, m1, &kf);
                     if (r < 0) continue;
@@ -79,11 +89,12 @@ __device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, in
     }
 }
 
-template <int R>
+template <int R, int M1S = 0>
 __device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys,
                                                 const float2* __restrict__ Zp, int H, int m1,
                                                 int m2, int P, int p,
                                                 const float2* __restrict__ tw_h) {
+    if (M1S) m1 = M1S;
     constexpr int Bq = ColCfg<R>::Bq;
     constexpr int J = 16 / Bq;
     constexpr int CP = ColCfg<R>::CP;
@@ -103,7 +114,7 @@ __device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys,
 #pragma unroll
                 for (int k1 = 0; k1 < Bq; ++k1) {
                     int kf;
-                    const int r = row_of_residue(16 * k1 + kk, R, H, m1, &kf);
+                    const int r = k1_live<R, M1S>(k1) ? row_of_residue(16 * k1 + kk, R, H, m1, &kf) : -1;
                     float2 val = make_float2(0.f, 0.f);
                     if (r >= 0) {
                         val = __ldg(&Zp[(size_t)r * m2 + col]);

@@ -6,7 +6,7 @@
 // A CTA owns 4 consecutive modes m0..m0+3, OC output channels (one thread
 // each) and BT batch rows:
 //   * w is viewed as a 3D tensor [Cin][Cout][2*NM floats] and X as
-//     [B][Cin][2*NM floats]; both stream through a 6-deep ring of shared-memory
+//     [B][Cin][2*NM floats]; both stream through a 4- or 6-deep ring of shared-memory
 //     stages, one TMA box of each per stage (w: 4 modes x OC x IC, X: 4 modes x
 //     IC x BT), completion tracked by one mbarrier per stage;
 //   * X values are read with broadcast loads (all lanes of a warp want the same
@@ -22,10 +22,10 @@
 namespace fno {
 namespace {
 
-constexpr int kStages = 6;
+constexpr int kMaxStages = 6;
 
 struct MixTmaCfg {
-    int OC, IC, BT, BTT, NBH, OT;
+    int OC, IC, BT, BTT, NBH, OT, NST;
     size_t w_off, x_off, stage_bytes, smem;
 };
 
@@ -46,7 +46,10 @@ MixTmaCfg mix_tma_cfg(int B, int Cin, int Cout) {
     c.w_off = 0;
     c.x_off = (size_t)32 * c.OC * c.IC;
     c.stage_bytes = c.x_off + (size_t)32 * c.IC * c.BT;
-    c.smem = 128 + (size_t)kStages * round128(c.stage_bytes);
+    // ring depth: 4 stages when the batch tile is large (more CTAs per SM for
+    // the FMA-heavy case), 6 when the weights stream nearly unused (HBM-bound)
+    c.NST = c.BT >= 8 ? 4 : kMaxStages;
+    c.smem = 128 + (size_t)c.NST * round128(c.stage_bytes);
     return c;
 }
 
@@ -56,7 +59,7 @@ template <int BTT, int OT>
 __global__ void __launch_bounds__(256)
 mix_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                float2* __restrict__ Z, int B, int Cin, int Cout, int NM, int OC, int IC, int BT,
-               unsigned* __restrict__ err) {
+               int kStages, unsigned* __restrict__ err) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     unsigned char* stages = smem + 128;
@@ -187,10 +190,10 @@ cudaError_t launch_btt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, 
     const int threads = c.OC / c.OT * c.NBH;
     if (c.OT == 2)
         mix_tma_kernel<BTT, 2><<<grid, threads, c.smem, s>>>(mw, mx, Z, B, Cin, Cout, NM, c.OC,
-                                                             c.IC, c.BT, err);
+                                                             c.IC, c.BT, c.NST, err);
     else
         mix_tma_kernel<BTT, 1><<<grid, threads, c.smem, s>>>(mw, mx, Z, B, Cin, Cout, NM, c.OC,
-                                                             c.IC, c.BT, err);
+                                                             c.IC, c.BT, c.NST, err);
     return cudaGetLastError();
 }
 

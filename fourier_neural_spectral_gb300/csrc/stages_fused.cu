@@ -87,13 +87,17 @@ __device__ __forceinline__ int pair_b(int p) { return p == 0 ? 8 : 16 - p; }
 // One packed row pair through the forward row transform.  Called by every lane
 // of the warp (the group of Bq lanes is inside one warp); `active` lanes do work.
 // Writes the separated spectra of the two rows, bins k < m2, to Ya and Yb.
-template <int W>
+template <int W, int M2S = 0>
 __device__ __forceinline__ void row_pair_forward(const float* __restrict__ ra,
                                                  const float* __restrict__ rb, float2* S,
                                                  float2* Ya, float2* Yb, int t, int m2,
                                                  const float2* __restrict__ tw, bool active) {
     constexpr int Bq = W / 16;
     constexpr int RS = Bq + 1;
+    // k1 blocks that can hold a kept bin k < m2 (all of them when m2 is known
+    // only at run time)
+    constexpr int KH = M2S > 0 ? (M2S + 15) / 16 : Bq;
+    if (M2S) m2 = M2S;
     if (active) {
         float2 v[16];
 #pragma unroll
@@ -154,6 +158,7 @@ __device__ __forceinline__ void row_pair_forward(const float* __restrict__ ra,
                 const int ka = pair_a(p), kb = pair_b(p);
 #pragma unroll
                 for (int k1 = 0; k1 < Bq; ++k1) {
+                    if (k1 >= KH) continue;
                     // X_a[k] = (Z[k] + conj Z[W-k]) / 2,  X_b[k] = (Z[k] - conj Z[W-k]) / 2i
                     const int k = 16 * k1 + ka;
                     if (k < m2) {
@@ -177,7 +182,7 @@ __device__ __forceinline__ void row_pair_forward(const float* __restrict__ ra,
 
 // One row pair through the inverse (complex-to-real) row transform: reads the
 // kept bins of rows a and b from Va, Vb and writes the two output rows.
-template <int W>
+template <int W, int M2S = 0>
 __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2* Vb, float2* S,
                                                  float* __restrict__ ya, float* __restrict__ yb,
                                                  int t, int m2, const float2* __restrict__ tw,
@@ -185,6 +190,8 @@ __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2*
     constexpr int Bq = W / 16;
     constexpr int RS = 17;
     constexpr int half = W / 2;
+    constexpr int KH = M2S > 0 ? (M2S + 15) / 16 : Bq;  // k1 blocks holding bins k < m2
+    if (M2S) m2 = M2S;
     if (active) {
         if constexpr (Bq == 16) {
             const int kk = t;
@@ -216,6 +223,7 @@ __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2*
                 for (int j = 0; j < Bq; ++j) ua[j] = ub[j] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k1 = 0; k1 < Bq; ++k1) {
+                    if (k1 >= KH) continue;      // only bins k < m2 carry data (mirrors below)
                     const int k = 16 * k1 + ka;  // its mirror W - k is bin kb (ka if p = 0)
                     if (k <= half && k < m2) {
                         float2 uk, um;
@@ -263,7 +271,7 @@ __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2*
 }
 
 // ---------------------------------------------------------------- forward ---
-template <int W, int R>
+template <int W, int R, int M1S = 0, int M2S = 0>
 __global__ void __launch_bounds__(kFT, (FusedCfg<W, R>::MinBlocks))
 fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m1, int m2,
                  int P, float scale, const float2* __restrict__ tw_w,
@@ -289,18 +297,19 @@ fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int
             const bool active = pair < npairs;
             const int qa = 2 * pair;
             const float* ra = xp + (size_t)(p + P * qa) * W;
-            row_pair_forward<W>(ra, ra + (size_t)P * W, S, Y + qa * ys, Y + (qa + 1) * ys, t, m2,
-                                tw_w, active);
+            row_pair_forward<W, M2S>(ra, ra + (size_t)P * W, S, Y + qa * ys, Y + (qa + 1) * ys, t,
+                                     m2, tw_w, active);
         }
     }
     __syncthreads();
 
     // ---- columns --------------------------------------------------------
-    columns_forward<R>(scr, Y, ys, X, (size_t)plane * 2 * m1 * m2, H, m1, m2, P, p, scale, tw_h);
+    columns_forward<R, M1S>(scr, Y, ys, X, (size_t)plane * 2 * m1 * m2, H, m1, m2, P, p, scale,
+                            tw_h);
 }
 
 // ---------------------------------------------------------------- inverse ---
-template <int W, int R>
+template <int W, int R, int M1S = 0, int M2S = 0>
 __global__ void __launch_bounds__(kFT, (FusedCfg<W, R>::MinBlocks))
 inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m1, int m2,
                  int P, float scale, const float2* __restrict__ tw_w,
@@ -316,7 +325,7 @@ inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int
     const float2* Zp = Z + (size_t)plane * R2 * m2;
 
     // ---- columns: retained rows of Z -> V[q][col], q in [0, R) ----------
-    columns_inverse<R>(scr, V, ys, Zp, H, m1, m2, P, p, tw_h);
+    columns_inverse<R, M1S>(scr, V, ys, Zp, H, m1, m2, P, p, tw_h);
     __syncthreads();
 
     // ---- rows: pairs of V rows -> two real output rows ------------------
@@ -332,11 +341,16 @@ inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int
             const bool active = pair < npairs;
             const int qa = 2 * pair;
             float* ya = yp + (size_t)(p + P * qa) * W;
-            row_pair_inverse<W>(V + qa * ys, V + (qa + 1) * ys, S, ya, ya + (size_t)P * W, t, m2,
-                                tw_w, scale, active);
+            row_pair_inverse<W, M2S>(V + qa * ys, V + (qa + 1) * ys, S, ya, ya + (size_t)P * W, t,
+                                     m2, tw_w, scale, active);
         }
     }
 }
+
+// Shapes with a kernel compiled for their (m1, m2): square planes with
+// m1 = m2 = W/4 (the retained block of the 64-, 128- and 256-point workloads).
+template <int W, int R>
+constexpr bool has_static() { return W == R && (W == 64 || W == 128 || W == 256); }
 
 __global__ void zero_kernel(float4* __restrict__ p, size_t n4) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
@@ -352,6 +366,15 @@ cudaError_t set_attrs() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(inv_fused_kernel<W, R>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if constexpr (has_static<W, R>()) {
+        const int sb = (int)std::min<size_t>(fused_smem_bytes<W, R>(W / 4), 227 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fwd_fused_kernel<W, R, W / 4, W / 4>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(inv_fused_kernel<W, R, W / 4, W / 4>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+    }
     return e;
 }
 
@@ -368,6 +391,13 @@ template <int W, int R>
 cudaError_t launch_fwd(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s) {
     const size_t smem = fused_smem_bytes<W, R>(p.m2);
     const unsigned grid = (unsigned)((size_t)p.B * p.Cin * p.P);
+    if constexpr (has_static<W, R>()) {
+        if (p.m1 == W / 4 && p.m2 == W / 4) {
+            fwd_fused_kernel<W, R, W / 4, W / 4><<<grid, kFT, smem, s>>>(
+                x, X, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w, p.tw_h);
+            return cudaGetLastError();
+        }
+    }
     fwd_fused_kernel<W, R><<<grid, kFT, smem, s>>>(x, X, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
                                                    p.tw_h);
     return cudaGetLastError();
@@ -377,6 +407,13 @@ template <int W, int R>
 cudaError_t launch_inv(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s) {
     const size_t smem = fused_smem_bytes<W, R>(p.m2);
     const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.P);
+    if constexpr (has_static<W, R>()) {
+        if (p.m1 == W / 4 && p.m2 == W / 4) {
+            inv_fused_kernel<W, R, W / 4, W / 4><<<grid, kFT, smem, s>>>(
+                Z, y, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w, p.tw_h);
+            return cudaGetLastError();
+        }
+    }
     inv_fused_kernel<W, R><<<grid, kFT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
                                                    p.tw_h);
     return cudaGetLastError();
