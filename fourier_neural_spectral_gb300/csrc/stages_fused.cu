@@ -72,10 +72,15 @@ struct FusedCfg {
     static constexpr int MinBlocks = W * R <= 128 * 128 ? 3 : (W * R <= 256 * 128 ? 2 : 1);
 };
 
+// Row stride of the kept-column array Y / V: m2 rounded up to == 4 (mod 8)
+// complex elements, so that the rows written (read) by neighbouring row-pair
+// groups fall on different shared-memory banks.
+__host__ __device__ inline int kept_stride(int m2) { return m2 + ((4 - m2 % 8) + 8) % 8; }
+
 template <int W, int R>
 size_t fused_smem_bytes(int m2) {
     using C = FusedCfg<W, R>;
-    return sizeof(float2) * ((size_t)C::Scratch + (size_t)R * (m2 + 1));
+    return sizeof(float2) * ((size_t)C::Scratch + (size_t)R * kept_stride(m2));
 }
 
 // Mirror partner of bin kk of the 16-point first pass: kk and (16 - kk) mod 16
@@ -87,11 +92,13 @@ __device__ __forceinline__ int pair_b(int p) { return p == 0 ? 8 : 16 - p; }
 // One packed row pair through the forward row transform.  Called by every lane
 // of the warp (the group of Bq lanes is inside one warp); `active` lanes do work.
 // Writes the separated spectra of the two rows, bins k < m2, to Ya and Yb.
+// tw1[kk] = e^{-2 pi i t kk / W}: the thread's first-pass twiddles, loaded once
+// per kernel and reused for every row pair.
 template <int W, int M2S = 0>
 __device__ __forceinline__ void row_pair_forward(const float* __restrict__ ra,
                                                  const float* __restrict__ rb, float2* S,
                                                  float2* Ya, float2* Yb, int t, int m2,
-                                                 const float2* __restrict__ tw, bool active) {
+                                                 const float2 (&tw1)[16], bool active) {
     constexpr int Bq = W / 16;
     constexpr int RS = Bq + 1;
     // k1 blocks that can hold a kept bin k < m2 (all of them when m2 is known
@@ -105,7 +112,7 @@ __device__ __forceinline__ void row_pair_forward(const float* __restrict__ ra,
             v[n2] = make_float2(__ldg(ra + t + Bq * n2), __ldg(rb + t + Bq * n2));
         dft<16, -1>(v);
 #pragma unroll
-        for (int kk = 1; kk < 16; ++kk) v[kk] = cmul(v[kk], root<-1>(tw, t * kk, W));
+        for (int kk = 1; kk < 16; ++kk) v[kk] = cmul(v[kk], tw1[kk]);
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) S[kk * RS + t] = v[kk];
     }
@@ -182,10 +189,34 @@ __device__ __forceinline__ void row_pair_forward(const float* __restrict__ ra,
 
 // One row pair through the inverse (complex-to-real) row transform: reads the
 // kept bins of rows a and b from Va, Vb and writes the two output rows.
+// The thread's first-pass twiddles e^{+2 pi i n1 kk / W} for its bins kk,
+// loaded once per kernel: twi[(ps * 2 + side) * Bq + n1] with side 0 for bin
+// pair_a(p), 1 for pair_b(p) (and twi[n1] = e^{+2 pi i n1 t / W} when Bq = 16).
+template <int W>
+__device__ __forceinline__ void inverse_twiddles(float2 (&twi)[16], int t,
+                                                 const float2* __restrict__ tw) {
+    constexpr int Bq = W / 16;
+    if constexpr (Bq == 16) {
+#pragma unroll
+        for (int n1 = 0; n1 < 16; ++n1) twi[n1] = root<1>(tw, n1 * t, W);
+    } else {
+        constexpr int NP = 8 / Bq;
+#pragma unroll
+        for (int ps = 0; ps < NP; ++ps) {
+            const int p = t + Bq * ps;
+#pragma unroll
+            for (int n1 = 0; n1 < Bq; ++n1) {
+                twi[(ps * 2) * Bq + n1] = root<1>(tw, n1 * pair_a(p), W);
+                twi[(ps * 2 + 1) * Bq + n1] = root<1>(tw, n1 * pair_b(p), W);
+            }
+        }
+    }
+}
+
 template <int W, int M2S = 0>
 __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2* Vb, float2* S,
                                                  float* __restrict__ ya, float* __restrict__ yb,
-                                                 int t, int m2, const float2* __restrict__ tw,
+                                                 int t, int m2, const float2 (&twi)[16],
                                                  float scale, bool active) {
     constexpr int Bq = W / 16;
     constexpr int RS = 17;
@@ -211,7 +242,7 @@ __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2*
             dft<16, 1>(u);
 #pragma unroll
             for (int n1 = 0; n1 < 16; ++n1)
-                S[n1 * RS + kk] = n1 == 0 ? u[0] : cmul(u[n1], root<1>(tw, n1 * kk, W));
+                S[n1 * RS + kk] = n1 == 0 ? u[0] : cmul(u[n1], twi[n1]);
         } else {
             constexpr int NP = 8 / Bq;
 #pragma unroll
@@ -249,8 +280,8 @@ __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2*
                 dft<Bq, 1>(ub);
 #pragma unroll
                 for (int n1 = 0; n1 < Bq; ++n1) {
-                    S[n1 * RS + ka] = n1 == 0 ? ua[0] : cmul(ua[n1], root<1>(tw, n1 * ka, W));
-                    S[n1 * RS + kb] = n1 == 0 ? ub[0] : cmul(ub[n1], root<1>(tw, n1 * kb, W));
+                    S[n1 * RS + ka] = n1 == 0 ? ua[0] : cmul(ua[n1], twi[(ps * 2) * Bq + n1]);
+                    S[n1 * RS + kb] = n1 == 0 ? ub[0] : cmul(ub[n1], twi[(ps * 2 + 1) * Bq + n1]);
                 }
             }
         }
@@ -280,7 +311,7 @@ fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int
     extern __shared__ float2 sm[];
     float2* scr = sm;
     float2* Y = sm + C::Scratch;  // [R][ys]
-    const int ys = m2 + 1;
+    const int ys = kept_stride(M2S ? M2S : m2);
     const int plane = blockIdx.x / P;
     const int p = blockIdx.x - plane * P;
     const float* xp = x + (size_t)plane * H * W;
@@ -290,6 +321,9 @@ fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int
         constexpr int Bq = C::BqW;
         const int g = threadIdx.x / Bq, t = threadIdx.x % Bq;
         float2* S = scr + g * C::RowScr;
+        float2 tw1[16];
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) tw1[kk] = root<-1>(tw_w, t * kk, W);
         constexpr int npairs = R / 2;
         constexpr int iters = (npairs + C::RowGroups - 1) / C::RowGroups;
         for (int it = 0; it < iters; ++it) {
@@ -298,7 +332,7 @@ fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int
             const int qa = 2 * pair;
             const float* ra = xp + (size_t)(p + P * qa) * W;
             row_pair_forward<W, M2S>(ra, ra + (size_t)P * W, S, Y + qa * ys, Y + (qa + 1) * ys, t,
-                                     m2, tw_w, active);
+                                     m2, tw1, active);
         }
     }
     __syncthreads();
@@ -318,7 +352,7 @@ inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int
     extern __shared__ float2 sm[];
     float2* scr = sm;
     float2* V = sm + C::Scratch;  // [R][ys]
-    const int ys = m2 + 1;
+    const int ys = kept_stride(M2S ? M2S : m2);
     const int plane = blockIdx.x / P;
     const int p = blockIdx.x - plane * P;
     const int R2 = 2 * m1;
@@ -333,6 +367,8 @@ inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int
         constexpr int Bq = C::BqW;
         const int g = threadIdx.x / Bq, t = threadIdx.x % Bq;
         float2* S = scr + g * C::RowScr;
+        float2 twi[16];
+        inverse_twiddles<W>(twi, t, tw_w);
         float* yp = y + (size_t)plane * H * W;
         constexpr int npairs = R / 2;
         constexpr int iters = (npairs + C::RowGroups - 1) / C::RowGroups;
@@ -342,7 +378,7 @@ inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int
             const int qa = 2 * pair;
             float* ya = yp + (size_t)(p + P * qa) * W;
             row_pair_inverse<W, M2S>(V + qa * ys, V + (qa + 1) * ys, S, ya, ya + (size_t)P * W, t,
-                                     m2, tw_w, scale, active);
+                                     m2, twi, scale, active);
         }
     }
 }
