@@ -104,10 +104,10 @@ __device__ __forceinline__ float2 root(const float2* __restrict__ tab, int j, in
 // Retained row r of the weight layout for true frequency k1, and back.
 __device__ __forceinline__ int freq_of_row(int r, int H, int m1) { return r < m1 ? r : H - 2 * m1 + r; }
 
-// For a column transform of length R over the rows p + P*q (H = P*R, R >= 2*m1),
-// output residue f in [0, R) holds true frequency k1 with k1 mod R == f.  Returns
-// the retained row r of that frequency, or -1 if no retained frequency has
-// residue f.  *k1 receives the true frequency.
+// For a column transform of length R over the rows p + P*q (H = P*R) with
+// R >= 2*m1, at most one retained frequency k1 has k1 mod R == f for an output
+// residue f in [0, R).  Returns the retained row r of that frequency, or -1 if
+// there is none.  *k1 receives the true frequency.
 __device__ __forceinline__ int row_of_residue(int f, int R, int H, int m1, int* k1) {
     if (f < m1) {
         *k1 = f;

@@ -118,7 +118,7 @@ void describe_fused(fno_plan_s* p) {
     int k = 0;
     if (p->P > 1) set_kernel(p, k++, "zero_X", X_bytes(p), 0);
     const double fl_f = Pi * (fft_flops(p->W) * p->H / 2 + fft_flops(p->R) * p->m2 * p->P);
-    const double fl_i = Po * (fft_flops(p->W) * p->H / 2 + fft_flops(p->R) * p->m2 * p->P);
+    const double fl_i = Po * (fft_flops(p->W) * p->H / 2 + fft_flops(p->Ri) * p->m2 * p->Pi);
     set_kernel(p, k++, "fwd_fused", x_bytes(p) + X_bytes(p), (size_t)fl_f);
     set_kernel(p, k++, mix_name(p), X_bytes(p) + w_bytes(p) + Z_bytes(p),
                8ull * p->B * p->Cin * p->Cout * p->nm);
@@ -195,10 +195,12 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     p->scale = (float)(1.0 / std::sqrt((double)H * (double)W));
     if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return FNO_ERR_CUDA; }
 
-    int R = 0;
-    p->path = fused_supported(W, H, m1, m2, &R) ? 1 : 0;
-    p->R = p->path == 1 ? R : H;
+    int Rf = 0, Ri = 0;
+    p->path = fused_supported(W, H, m1, m2, &Rf, &Ri) ? 1 : 0;
+    p->R = p->path == 1 ? Rf : H;
     p->P = H / p->R;
+    p->Ri = p->path == 1 ? Ri : H;
+    p->Pi = H / p->Ri;
     p->mix_path = mix_tma_supported(B, Cin, Cout, p->nm) ? 1 : 0;
     p->tc_split = prec == FNO_PREC_3XTF32 ? 3 : 1;
     // tensor cores for the contraction only where it is a real dense product
@@ -219,8 +221,8 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     if (p->path == 1) {
         describe_fused(p);
         std::snprintf(p->desc, sizeof(p->desc),
-                      "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|%s|inv-cols+rows", W, p->R,
-                      p->P, mix_name(p));
+                      "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|%s|inv-cols+rows(R=%d,P=%d)", W,
+                      p->R, p->P, mix_name(p), p->Ri, p->Pi);
     } else {
         describe_generic(p);
         std::snprintf(p->desc, sizeof(p->desc),

@@ -5,10 +5,15 @@
 // Forward: every kept column k2 of Y[q][k2] (q in [0, R)) is transformed with an
 // R-point DFT split as R = 16 * (R/16): a 16-point register DFT over the rows
 // q = n1 + (R/16)*n2, twiddle e^{-2 pi i n1 kk / R}, shared-memory transpose,
-// then (R/16)-point DFTs.  Output residue f holds the retained frequency k1
-// with k1 = f mod R (R >= 2*m1); it is scaled by 1/sqrt(HW) and stored to X
-// (P = 1) or multiplied by e^{-2 pi i k1 p / H} and added to X (P > 1).
-// Inverse: the mirror (decimation in time) with inputs read from Z.
+// then (R/16)-point DFTs.  With P = 1 (R = H) output residue f is the
+// frequency itself and is scaled by 1/sqrt(HW) and stored to X.  With P > 1 the
+// rows are h = p + P*q and, since H = P*R,
+//   X[k1] = sum_h Y[h] e^{-2 pi i k1 h / H}
+//         = e^{-2 pi i k1 p / H} * (R-point DFT over q)[k1 mod R],
+// so every retained k1 takes residue k1 mod R times its own twiddle and adds it
+// into X (R need not reach 2*m1: frequencies sharing a residue simply read the
+// same value).  Inverse: the mirror (decimation in time); with P > 1 the inputs
+// of a residue are the sum of its retained frequencies times e^{+2 pi i k1 p / H}.
 #pragma once
 
 #include "fft_reg.cuh"
@@ -70,17 +75,29 @@ __device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, in
 #pragma unroll
                 for (int k1 = 0; k1 < Bq; ++k1) {
                     if (!k1_live<R, M1S>(k1)) continue;
-                    int kf;
-                    const int r = row_of_residue(16 * k1 + kk, R, H, m1, &kf);
-                    if (r < 0) continue;
-                    float2 val = cscale(u[k1], scale);
-                    float2* dst = X + xbase + (size_t)r * m2 + col;
-                    if (P == 1) {
-                        *dst = val;
+                    const int f = 16 * k1 + kk;  // residue of the retained frequencies
+                    const float2 val = cscale(u[k1], scale);
+                    if (P == 1 || R >= 2 * m1) {
+                        // at most one retained frequency per residue
+                        int kf;
+                        const int r = row_of_residue(f, R, H, m1, &kf);
+                        if (r < 0) continue;
+                        float2* dst = X + xbase + (size_t)r * m2 + col;
+                        if (P == 1)
+                            *dst = val;
+                        else
+                            atomicAdd(reinterpret_cast<float2*>(dst),
+                                      cmul(val, root<-1>(tw_h, kf * p, H)));
                     } else {
-                        val = cmul(val, root<-1>(tw_h, kf * p, H));
-                        atomicAdd(&dst->x, val.x);
-                        atomicAdd(&dst->y, val.y);
+                        // every retained k1 == f (mod R): lower side f, f + R, ... < m1,
+                        // upper side H - R + f, H - 2R + f, ... >= H - m1
+                        for (int kf = f; kf < m1; kf += R)
+                            atomicAdd(reinterpret_cast<float2*>(X + xbase + (size_t)kf * m2 + col),
+                                      cmul(val, root<-1>(tw_h, kf * p, H)));
+                        for (int kf = H - R + f; kf >= H - m1; kf -= R)
+                            atomicAdd(reinterpret_cast<float2*>(
+                                          X + xbase + (size_t)(kf - H + 2 * m1) * m2 + col),
+                                      cmul(val, root<-1>(tw_h, kf * p, H)));
                     }
                 }
             }
@@ -113,12 +130,25 @@ __device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys,
                 float2 u[Bq];
 #pragma unroll
                 for (int k1 = 0; k1 < Bq; ++k1) {
-                    int kf;
-                    const int r = k1_live<R, M1S>(k1) ? row_of_residue(16 * k1 + kk, R, H, m1, &kf) : -1;
+                    const int f = 16 * k1 + kk;
                     float2 val = make_float2(0.f, 0.f);
-                    if (r >= 0) {
-                        val = __ldg(&Zp[(size_t)r * m2 + col]);
-                        if (P > 1) val = cmul(val, root<1>(tw_h, kf * p, H));
+                    if (k1_live<R, M1S>(k1)) {
+                        if (P == 1 || R >= 2 * m1) {
+                            int kf;
+                            const int r = row_of_residue(f, R, H, m1, &kf);
+                            if (r >= 0) {
+                                val = __ldg(&Zp[(size_t)r * m2 + col]);
+                                if (P > 1) val = cmul(val, root<1>(tw_h, kf * p, H));
+                            }
+                        } else {
+                            // sum of every retained k1 == f (mod R), each times e^{+2 pi i k1 p / H}
+                            for (int kf = f; kf < m1; kf += R)
+                                val = cadd(val, cmul(__ldg(&Zp[(size_t)kf * m2 + col]),
+                                                     root<1>(tw_h, kf * p, H)));
+                            for (int kf = H - R + f; kf >= H - m1; kf -= R)
+                                val = cadd(val, cmul(__ldg(&Zp[(size_t)(kf - H + 2 * m1) * m2 + col]),
+                                                     root<1>(tw_h, kf * p, H)));
+                        }
                     }
                     u[k1] = val;
                 }

@@ -47,7 +47,8 @@ struct fno_plan_s {
     int path;               // 0: shape-generic kernels, 1: fused transform kernels
     int mix_path;           // 0: mix_fma, 1: mix_tma (TMA-fed fp32), 2: mix_tc (tcgen05)
     int tc_split;           // mix_tc: 1 (TF32) or 3 (split TF32, hi*hi + hi*lo + lo*hi)
-    int R, P;               // fused path: column length per CTA and H / R
+    int R, P;               // fused path, forward: column length per CTA and H / R
+    int Ri, Pi;             // fused path, inverse: the same
     int launches;           // kernel launches per execute
     fno_kernel_desc kernels[kMaxKernels];
     cudaEvent_t* events;    // armed per-kernel timing events (count = launches + 1)
@@ -61,7 +62,7 @@ cudaError_t mix_init();
 
 // Fused transform kernels (stages_fused.cu).
 cudaError_t stages_fused_init();
-bool fused_supported(int W, int H, int m1, int m2, int* R_out);
+bool fused_supported(int W, int H, int m1, int m2, int* R_fwd, int* R_inv);
 size_t fused_smem_bytes_any(int W, int R, int m2);
 cudaError_t launch_forward_fused(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s,
                                  fno_launch_ctx* ctx);

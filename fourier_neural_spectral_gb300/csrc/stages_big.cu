@@ -31,7 +31,6 @@ namespace fno {
 namespace {
 
 constexpr int kBT = 256;      // threads per CTA
-constexpr int kPrefetch = 4;  // row pairs a group asks L2 to fetch ahead of use
 constexpr int kNL = 4;        // candidate k1 per side: ceil(m2 / 16) <= 4, i.e. m2 <= 64
 
 template <int W>
@@ -126,21 +125,10 @@ fwd_big_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m
 
     constexpr int npairs = R / 2;
     constexpr int iters = (npairs + B::Groups - 1) / B::Groups;
-    // rows of pair j of this group: p + P*(2j) and p + P*(2j + 1)
-    auto prefetch_pair = [&](int pr) {
-        if (pr < npairs) {
-            const float* r0 = xp + (size_t)(p + P * 2 * pr) * W;
-            prefetch_l2_bulk(r0, W * sizeof(float));
-            prefetch_l2_bulk(r0 + (size_t)P * W, W * sizeof(float));
-        }
-    };
-    if (t == 0)
-        for (int d = 1; d <= kPrefetch; ++d) prefetch_pair(g + d * B::Groups);
     for (int it = 0; it < iters; ++it) {
         const int pair = g + it * B::Groups;
         const bool active = pair < npairs;  // uniform over the group
         const int qa = 2 * pair;
-        if (t == 0) prefetch_pair(pair + (kPrefetch + 1) * B::Groups);
         if (active) {
             const float* ra = xp + (size_t)(p + P * qa) * W;
             const float* rb = ra + (size_t)P * W;
@@ -297,8 +285,8 @@ cudaError_t launch(const fno_plan_s& p, const float* x, float2* X, const float2*
         fwd_big_kernel<W, R><<<grid, kBT, smem, s>>>(x, X, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
                                                      p.tw_h);
     } else {
-        const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.P);
-        inv_big_kernel<W, R><<<grid, kBT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
+        const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.Pi);
+        inv_big_kernel<W, R><<<grid, kBT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w,
                                                      p.tw_h);
     }
     return cudaGetLastError();
@@ -307,7 +295,7 @@ cudaError_t launch(const fno_plan_s& p, const float* x, float2* X, const float2*
 template <bool FWD, int W>
 cudaError_t dispatch_r(const fno_plan_s& p, const float* x, float2* X, const float2* Z, float* y,
                        cudaStream_t s) {
-    switch (p.R) {
+    switch (FWD ? p.R : p.Ri) {
         case 32: return launch<FWD, W, 32>(p, x, X, Z, y, s);
         case 64: return launch<FWD, W, 64>(p, x, X, Z, y, s);
         case 128: return launch<FWD, W, 128>(p, x, X, Z, y, s);

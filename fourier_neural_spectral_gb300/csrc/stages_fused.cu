@@ -442,15 +442,15 @@ cudaError_t launch_fwd(const fno_plan_s& p, const float* x, float2* X, cudaStrea
 template <int W, int R>
 cudaError_t launch_inv(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s) {
     const size_t smem = fused_smem_bytes<W, R>(p.m2);
-    const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.P);
+    const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.Pi);
     if constexpr (has_static<W, R>()) {
         if (p.m1 == W / 4 && p.m2 == W / 4) {
             inv_fused_kernel<W, R, W / 4, W / 4><<<grid, kFT, smem, s>>>(
-                Z, y, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w, p.tw_h);
+                Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h);
             return cudaGetLastError();
         }
     }
-    inv_fused_kernel<W, R><<<grid, kFT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
+    inv_fused_kernel<W, R><<<grid, kFT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w,
                                                    p.tw_h);
     return cudaGetLastError();
 }
@@ -458,7 +458,7 @@ cudaError_t launch_inv(const fno_plan_s& p, const float2* Z, float* y, cudaStrea
 template <bool FWD, int W>
 cudaError_t dispatch_r(const fno_plan_s& p, const float* x, float2* X, const float2* Z, float* y,
                        cudaStream_t s) {
-    switch (p.R) {
+    switch (FWD ? p.R : p.Ri) {
         case 32: return FWD ? launch_fwd<W, 32>(p, x, X, s) : launch_inv<W, 32>(p, Z, y, s);
         case 64: return FWD ? launch_fwd<W, 64>(p, x, X, s) : launch_inv<W, 64>(p, Z, y, s);
         case 128: return FWD ? launch_fwd<W, 128>(p, x, X, s) : launch_inv<W, 128>(p, Z, y, s);
@@ -494,21 +494,28 @@ cudaError_t stages_fused_init() {
 
 size_t fused_smem_bytes_any(int W, int R, int m2);
 
-bool fused_supported(int W, int H, int m1, int m2, int* R_out) {
+bool fused_supported(int W, int H, int m1, int m2, int* R_fwd, int* R_inv) {
     if (W < 32 || H < 32) return false;
     if (W > 256 && m2 > 64) return false;  // long rows keep at most 64 columns
-    // the column length R: the whole column when it fits, else the smallest
-    // power of two >= max(2*m1, 32) that divides H, at most 256
-    int R = H <= 256 ? H : 0;
-    if (!R) {
-        R = 32;
-        while (R < 2 * m1) R <<= 1;
-        if (R > 256) return false;
+    // the column length R: the whole column when it fits (P = 1), else strided
+    // row groups h = p + P*q of R rows per CTA (the forward adds its groups into
+    // X with atomics; retained frequencies sharing a residue mod R read the
+    // same value, so R need not reach 2*m1).  Measured at 2048 x 2048, m1 = 64:
+    // forward R = 32 / 64 / 128 -> 414 / 299 / 339 us, inverse R = 64 / 128 /
+    // 256 -> 340 / 297 / 425 us.
+    int Rf = H, Ri = H;
+    if (H > 256) {
+        Rf = 64;
+        Ri = 32;
+        while (Ri < 2 * m1 && Ri < 128) Ri <<= 1;
     }
-    if (R < 2 * m1 || R > H) return false;
-    const size_t smem = W <= 256 ? fused_smem_bytes_any(W, R, m2) : big_smem_bytes_any(W, R, m2);
-    if (smem > 227 * 1024) return false;
-    *R_out = R;
+    if (H <= 256 && H < 2 * m1) return false;
+    const auto smem = [&](int R) {
+        return W <= 256 ? fused_smem_bytes_any(W, R, m2) : big_smem_bytes_any(W, R, m2);
+    };
+    if (smem(Rf) > 227 * 1024 || smem(Ri) > 227 * 1024) return false;
+    *R_fwd = Rf;
+    *R_inv = Ri;
     return true;
 }
 

@@ -22,13 +22,16 @@ EDGE_SHAPES = [
     (1, 1, 1, 4096, 2, 1, 1),       # longest column transform
     (1, 1, 2, 2, 4096, 1, 2049),    # longest row transform, every column kept
     (2, 33, 31, 32, 32, 7, 9),      # channel counts off the tile sizes
-    # fused transform path: row groups h = p + P*q with P > 1, Nyquist, non-square
-    (2, 3, 4, 512, 64, 16, 9),      # R = 32, P = 16
-    (1, 2, 2, 1024, 128, 64, 65),   # R = 128, P = 8, Nyquist column kept
+    # fused transform path: row groups h = p + P*q with P > 1 (forward R = 64,
+    # inverse R = 32..128 once H > 256), Nyquist, non-square
+    (2, 3, 4, 512, 64, 16, 9),      # fwd P = 8, inv R = 32, P = 16
+    (1, 2, 2, 1024, 128, 64, 65),   # two retained frequencies per forward residue, Nyquist kept
     (2, 4, 4, 64, 256, 32, 129),    # 2*m1 = H, m2 = W/2 + 1
     (2, 3, 5, 256, 32, 128, 17),    # every row retained, narrow rows
     (3, 2, 3, 128, 64, 5, 7),       # odd mode counts inside the fused path
-    (2, 4, 6, 2048, 32, 64, 16),    # tall grid: R = 128, P = 16
+    (2, 4, 6, 2048, 32, 64, 16),    # tall grid: fwd P = 32, inv P = 16
+    (1, 2, 3, 1024, 64, 100, 7),    # m1 off the column length: 1 or 2 frequencies per residue
+    (2, 2, 2, 512, 32, 256, 5),     # 2*m1 = H with P > 1: 8 frequencies per forward residue
     # TMA-fed contraction: ragged boxes
     (3, 33, 40, 32, 32, 3, 5),      # B < batch tile, Cin % IC != 0, Cout % 32 != 0, NM % 4 == 2
     (5, 16, 96, 64, 32, 4, 4),      # B = 5 -> batch tile 8 split over two warp groups
@@ -37,7 +40,7 @@ EDGE_SHAPES = [
     (2, 3, 4, 64, 512, 16, 33),     # W = 512
     (1, 2, 2, 32, 1024, 8, 64),     # W = 1024, the largest supported m2
     (1, 1, 2, 256, 4096, 32, 17),   # W = 4096, one row group per CTA
-    (2, 2, 3, 512, 2048, 128, 5),   # 2*m1 = 256 -> R = 256, P = 2
+    (2, 2, 3, 512, 2048, 128, 5),   # 2*m1 = 256 > both column lengths
     (1, 3, 3, 1024, 2048, 64, 1),   # a single kept column
 ]
 
