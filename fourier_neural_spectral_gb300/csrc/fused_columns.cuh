@@ -50,6 +50,7 @@ __device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, in
     const int cs = threadIdx.x % CP;   // column within the pass
     const int n1 = threadIdx.x / CP;   // position within the column transform
     float2* S = scr + cs * ColCfg<R>::Scr;  // S[kk][n1] with row stride Bq
+    const float2 cdn = root<-1>(tw_h, (H - R) * p, H);  // e^{-2 pi i (H - R) p / H}
     for (int c0 = 0; c0 < m2; c0 += CP) {
         const int col = c0 + cs;
         const bool active = col < m2;
@@ -77,17 +78,22 @@ __device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, in
                     if (!k1_live<R, M1S>(k1)) continue;
                     const int f = 16 * k1 + kk;  // residue of the retained frequencies
                     const float2 val = cscale(u[k1], scale);
-                    if (P == 1 || R >= 2 * m1) {
-                        // at most one retained frequency per residue
+                    if (P == 1) {
                         int kf;
                         const int r = row_of_residue(f, R, H, m1, &kf);
-                        if (r < 0) continue;
-                        float2* dst = X + xbase + (size_t)r * m2 + col;
-                        if (P == 1)
-                            *dst = val;
-                        else
-                            atomicAdd(reinterpret_cast<float2*>(dst),
-                                      cmul(val, root<-1>(tw_h, kf * p, H)));
+                        if (r >= 0) X[xbase + (size_t)r * m2 + col] = val;
+                    } else if (m1 <= R) {
+                        // at most one retained frequency per side: lower k1 = f, upper
+                        // k1 = H - R + f, whose twiddle is the lower one times cdn
+                        const bool lo = f < m1, hi = f >= R - m1;
+                        if (!lo && !hi) continue;
+                        const float2 a = cmul(val, root<-1>(tw_h, f * p, H));
+                        if (lo)
+                            atomicAdd(reinterpret_cast<float2*>(X + xbase + (size_t)f * m2 + col), a);
+                        if (hi)
+                            atomicAdd(reinterpret_cast<float2*>(
+                                          X + xbase + (size_t)(f - R + 2 * m1) * m2 + col),
+                                      cmul(a, cdn));
                     } else {
                         // every retained k1 == f (mod R): lower side f, f + R, ... < m1,
                         // upper side H - R + f, H - 2R + f, ... >= H - m1
@@ -106,10 +112,42 @@ __device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, in
     }
 }
 
-template <int R, int M1S = 0>
-__device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys,
-                                                const float2* __restrict__ Zp, int H, int m1,
-                                                int m2, int P, int p,
+// Input residue f of the inverse column transform of the row group p: the
+// sum of Z over the retained k1 == f (mod R), each times e^{+2 pi i k1 p / H}
+// (P = 1: the single retained frequency k1 = f, if any).  `cup` is
+// e^{+2 pi i (H - R) p / H}, the ratio of the upper-side twiddle to the lower.
+// ZS: Z is in shared memory (plain loads) rather than global memory.
+template <int R, bool ZS>
+__device__ __forceinline__ float2 gather_residue(const float2* Zp, int f, int col, int H, int m1,
+                                                 int m2, int P, int p, float2 cup,
+                                                 const float2* __restrict__ tw_h) {
+    const auto ld = [&](size_t i) { return ZS ? Zp[i] : __ldg(&Zp[i]); };
+    float2 val = make_float2(0.f, 0.f);
+    if (P == 1) {
+        int kf;
+        const int r = row_of_residue(f, R, H, m1, &kf);
+        if (r >= 0) val = ld((size_t)r * m2 + col);
+    } else if (m1 <= R) {
+        // at most one retained frequency per side: lower k1 = f, upper k1 = H - R + f
+        const bool lo = f < m1, hi = f >= R - m1;
+        float2 s = lo ? ld((size_t)f * m2 + col) : make_float2(0.f, 0.f);
+        if (hi) s = cadd(s, cmul(ld((size_t)(f - R + 2 * m1) * m2 + col), cup));
+        if (lo || hi) val = cmul(s, root<1>(tw_h, f * p, H));
+    } else {
+        for (int kf = f; kf < m1; kf += R)
+            val = cadd(val, cmul(ld((size_t)kf * m2 + col), root<1>(tw_h, kf * p, H)));
+        for (int kf = H - R + f; kf >= H - m1; kf -= R)
+            val = cadd(val, cmul(ld((size_t)(kf - H + 2 * m1) * m2 + col), root<1>(tw_h, kf * p, H)));
+    }
+    return val;
+}
+
+// ZS = true: Zp points to the plane's Z in shared memory, overlapping scr and V;
+// requires a single pass (m2 <= ColCfg<R>::CP).  Every thread reads its inputs
+// before the first barrier, after which the scratch and V may be rewritten.
+template <int R, int M1S = 0, bool ZS = false>
+__device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys, const float2* Zp,
+                                                int H, int m1, int m2, int P, int p,
                                                 const float2* __restrict__ tw_h) {
     if (M1S) m1 = M1S;
     constexpr int Bq = ColCfg<R>::Bq;
@@ -118,44 +156,34 @@ __device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys,
     const int cs = threadIdx.x % CP;
     const int t = threadIdx.x / CP;
     float2* S = scr + cs * ColCfg<R>::Scr;  // S[n1][kk] with row stride 16
+    const float2 cup = root<1>(tw_h, (H - R) * p, H);
     for (int c0 = 0; c0 < m2; c0 += CP) {
         const int col = c0 + cs;
         const bool active = col < m2;
+        // the inputs U[16*k1 + kk] for kk = t + Bq*j
+        float2 u[J][Bq];
+        if (active) {
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+#pragma unroll
+                for (int k1 = 0; k1 < Bq; ++k1)
+                    u[j][k1] = k1_live<R, M1S>(k1)
+                                   ? gather_residue<R, ZS>(Zp, 16 * k1 + t + Bq * j, col, H, m1,
+                                                           m2, P, p, cup, tw_h)
+                                   : make_float2(0.f, 0.f);
+        }
+        if (ZS) __syncthreads();  // Z fully read before the scratch is rewritten
         if (active) {
             // pass 1 (transposed): for kk = t + Bq*j, inverse Bq-point DFT over
-            // k1 of U[16*k1 + kk], then times e^{+2 pi i n1 kk / R}
+            // k1, then times e^{+2 pi i n1 kk / R}
 #pragma unroll
             for (int j = 0; j < J; ++j) {
                 const int kk = t + Bq * j;
-                float2 u[Bq];
-#pragma unroll
-                for (int k1 = 0; k1 < Bq; ++k1) {
-                    const int f = 16 * k1 + kk;
-                    float2 val = make_float2(0.f, 0.f);
-                    if (k1_live<R, M1S>(k1)) {
-                        if (P == 1 || R >= 2 * m1) {
-                            int kf;
-                            const int r = row_of_residue(f, R, H, m1, &kf);
-                            if (r >= 0) {
-                                val = __ldg(&Zp[(size_t)r * m2 + col]);
-                                if (P > 1) val = cmul(val, root<1>(tw_h, kf * p, H));
-                            }
-                        } else {
-                            // sum of every retained k1 == f (mod R), each times e^{+2 pi i k1 p / H}
-                            for (int kf = f; kf < m1; kf += R)
-                                val = cadd(val, cmul(__ldg(&Zp[(size_t)kf * m2 + col]),
-                                                     root<1>(tw_h, kf * p, H)));
-                            for (int kf = H - R + f; kf >= H - m1; kf -= R)
-                                val = cadd(val, cmul(__ldg(&Zp[(size_t)(kf - H + 2 * m1) * m2 + col]),
-                                                     root<1>(tw_h, kf * p, H)));
-                        }
-                    }
-                    u[k1] = val;
-                }
-                dft<Bq, 1>(u);
+                dft<Bq, 1>(u[j]);
 #pragma unroll
                 for (int n1 = 0; n1 < Bq; ++n1) {
-                    const float2 w = n1 == 0 ? u[n1] : cmul(u[n1], root<1>(tw_h, n1 * kk * P, H));
+                    const float2 w =
+                        n1 == 0 ? u[j][n1] : cmul(u[j][n1], root<1>(tw_h, n1 * kk * P, H));
                     S[n1 * 16 + kk] = w;
                 }
             }

@@ -70,7 +70,8 @@ cudaError_t launch_inverse_fused(const fno_plan_s& p, const float2* Z, float* y,
                                  fno_launch_ctx* ctx);
 // Long-row variants (stages_big.cu), W in {512, 1024, 2048, 4096}, m2 <= 64.
 cudaError_t stages_big_init();
-size_t big_smem_bytes_any(int W, int R, int m2);
+size_t big_smem_bytes_any(int W, int R, int m2, bool fwd);
+bool big_z_staged_any(int W, int R, int m1, int m2);
 cudaError_t launch_forward_big(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s);
 cudaError_t launch_inverse_big(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s);
 

@@ -7,9 +7,12 @@
 //
 // Forward row transform of the packed pair z = x_a + i x_b, pruned to the bins
 // k < m2 and k > W - m2 (decimation in frequency, W = 16 * L):
-//   pass 1: thread n1 < L loads z[n1 + L*n2] (n2 < 16; consecutive threads read
-//           consecutive words), 16-point register DFT over n2, times
-//           e^{-2 pi i n1 kk / W}, stored as S[kk][n1];
+//   staging: one thread of the group copies the pair's two rows into shared
+//           memory with bulk asynchronous copies, one pair ahead, so that the
+//           loads overlap the previous pair's arithmetic;
+//   pass 1: thread n1 < L reads z[n1 + L*n2] (n2 < 16) from the staged rows,
+//           16-point register DFT over n2, times e^{-2 pi i n1 kk / W}, stored
+//           as S[kk][n1];
 //   pass 2: for each kk, the L-point DFT over n1 is needed only at the few
 //           k1 with 16*k1 + kk kept.  With n1 = a + G*b (G = L/16 lanes, b < 16),
 //             Zk[k1] = sum_a e^{-2 pi i a k1 / L} D_a[k1 mod 16],
@@ -50,9 +53,21 @@ struct BigKCfg {
                                        : ColCfg<R>::Scratch;
 };
 
-template <int W, int R>
+// Shared memory: column/row scratch | Y or V [R][m2 + 1] (rounded to 16 bytes) |
+// forward: the staged row pair of every group [Groups][2W] floats and one
+// mbarrier per group; inverse: one mbarrier (the plane's Z, staged over the
+// scratch and V when it fits).
+constexpr size_t kStageBytesPerCta = 256 * 32 * sizeof(float);  // Groups * 2W floats
+
+__host__ __device__ __forceinline__ size_t big_y_floats2(int R, int m2) {
+    return ((size_t)R * (m2 + 1) + 1) & ~(size_t)1;
+}
+
+template <int W, int R, bool FWD>
 size_t big_smem_bytes(int m2) {
-    return sizeof(float2) * ((size_t)BigKCfg<W, R>::Scratch + (size_t)R * (m2 + 1));
+    const size_t base = sizeof(float2) * ((size_t)BigKCfg<W, R>::Scratch + big_y_floats2(R, m2));
+    return FWD ? base + kStageBytesPerCta + sizeof(uint64_t) * BigCfg<W>::Groups
+               : base + sizeof(uint64_t);
 }
 
 // Synchronise the L threads of a row-pair group.
@@ -100,18 +115,42 @@ __device__ __forceinline__ void reduce_scatter(float2 (&r)[N], int a) {
 template <int W, int R>
 __global__ void __launch_bounds__(kBT, 2)
 fwd_big_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m1, int m2, int P,
-               float scale, const float2* __restrict__ tw_w, const float2* __restrict__ tw_h) {
+               float scale, const float2* __restrict__ tw_w, const float2* __restrict__ tw_h,
+               unsigned* __restrict__ err) {
     using B = BigCfg<W>;
     constexpr int L = B::L, G = B::G, NK = B::NK;
-    extern __shared__ float2 sm[];
+    constexpr uint32_t kRowBytes = W * sizeof(float);
+    static_assert(B::Groups * 2 * kRowBytes == kStageBytesPerCta, "stage size");
+    static_assert(BigKCfg<W, R>::Scratch % 2 == 0, "stage must start on 16 bytes");
+    extern __shared__ __align__(16) float2 sm[];
     float2* scr = sm;
     float2* Y = sm + BigKCfg<W, R>::Scratch;  // [R][ys]
+    float* stage = reinterpret_cast<float*>(Y + big_y_floats2(R, m2));  // [Groups][2W]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage + B::Groups * 2 * W);
     const int ys = m2 + 1;
     const int plane = blockIdx.x / P;
     const int p = blockIdx.x - plane * P;
     const float* xp = x + (size_t)plane * H * W;
 
     const int g = threadIdx.x / L, t = threadIdx.x % L;
+    constexpr int npairs = R / 2;
+    float* stg = stage + g * 2 * W;
+    uint64_t* bar = bars + g;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < B::Groups; ++i) mbar_init(&bars[i], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // rows p + P*2*pair and p + P*(2*pair + 1) into the group's stage
+    const auto issue = [&](int pair) {
+        const float* ra = xp + (size_t)(p + P * 2 * pair) * W;
+        mbar_arrive_expect_tx(bar, 2 * kRowBytes);
+        bulk_load(stg, ra, kRowBytes, bar);
+        bulk_load(stg + W, ra + (size_t)P * W, kRowBytes, bar);
+    };
+    bool live = true;     // no wait of this thread has run out
+    int pending = -1;     // thread t == 0: parity of a copy that was never seen to land
+    if (t == 0 && g < npairs) issue(g);
     float2* S = scr + g * B::GroupScr;  // S[kk][n1], row stride L + G
     float2* Zs = S + 16 * B::SStride;   // Zs[kk][slot]
     // pass-1 twiddles e^{-2 pi i n1 kk / W} for n1 = t, and pass-2 twiddles
@@ -123,25 +162,30 @@ fwd_big_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m
 #pragma unroll
     for (int j = 0; j < NK; ++j) tw2[j] = root<-1>(tw_w, 16 * a * cand_k1<L>(j), W);
 
-    constexpr int npairs = R / 2;
     constexpr int iters = (npairs + B::Groups - 1) / B::Groups;
     for (int it = 0; it < iters; ++it) {
         const int pair = g + it * B::Groups;
         const bool active = pair < npairs;  // uniform over the group
         const int qa = 2 * pair;
         if (active) {
-            const float* ra = xp + (size_t)(p + P * qa) * W;
-            const float* rb = ra + (size_t)P * W;
+            if (live && !wait_parity_bounded(bar, (uint32_t)(it & 1), err)) {
+                live = false;  // the stage holds no valid data; err is set
+                if (t == 0) pending = it & 1;
+            }
             float2 v[16];
 #pragma unroll
-            for (int n2 = 0; n2 < 16; ++n2)
-                v[n2] = make_float2(__ldg(ra + t + L * n2), __ldg(rb + t + L * n2));
+            for (int n2 = 0; n2 < 16; ++n2) v[n2] = make_float2(stg[t + L * n2], stg[W + t + L * n2]);
             dft<16, -1>(v);
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk)
                 S[kk * B::SStride + t] = kk == 0 ? v[0] : cmul(v[kk], tw1[kk]);
         }
         group_sync<L>(g);
+        // every thread of the group has read the stage: refill it with the next pair
+        if (t == 0 && live && pair + B::Groups < npairs) {
+            fence_proxy_async_smem();
+            issue(pair + B::Groups);
+        }
         if (active) {
             float2 d[16];
 #pragma unroll
@@ -176,19 +220,32 @@ fwd_big_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m
         // the next pair's pass 1 rewrites S only; S was last read before the
         // second barrier above, and Zs is rewritten only after the next first barrier
     }
+    // a copy that ran out of time may still land: wait for it (bounded) before
+    // the shared memory is reused or released
+    if (pending >= 0) wait_parity_bounded(bar, (uint32_t)pending, nullptr);
     __syncthreads();
     columns_forward<R>(scr, Y, ys, X, (size_t)plane * 2 * m1 * m2, H, m1, m2, P, p, scale, tw_h);
 }
 
 // ---------------------------------------------------------------- inverse ---
+// Whether the plane's Z (16*m1*m2 bytes, contiguous) is brought into shared
+// memory with one bulk copy: the column transform must take a single pass and
+// Z must fit over the scratch and V, which it overwrites only after it is read.
 template <int W, int R>
+__host__ __device__ bool big_z_staged(int m1, int m2) {
+    return m2 <= ColCfg<R>::CP &&
+           16ull * m1 * m2 <= sizeof(float2) * (BigKCfg<W, R>::Scratch + big_y_floats2(R, m2));
+}
+
+template <int W, int R, bool ZS>
 __global__ void __launch_bounds__(kBT, 2)
 inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m1, int m2, int P,
-               float scale, const float2* __restrict__ tw_w, const float2* __restrict__ tw_h) {
+               float scale, const float2* __restrict__ tw_w, const float2* __restrict__ tw_h,
+               unsigned* __restrict__ err) {
     using B = BigCfg<W>;
     constexpr int L = B::L, G = B::G, NK = B::NK;
     constexpr int half = W / 2;
-    extern __shared__ float2 sm[];
+    extern __shared__ __align__(16) float2 sm[];
     float2* scr = sm;
     float2* V = sm + BigKCfg<W, R>::Scratch;  // [R][ys]
     const int ys = m2 + 1;
@@ -196,17 +253,39 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
     const int p = blockIdx.x - plane * P;
     const float2* Zp = Z + (size_t)plane * 2 * m1 * m2;
 
-    columns_inverse<R>(scr, V, ys, Zp, H, m1, m2, P, p, tw_h);
+    // ZS (big_z_staged): the plane's Z comes into shared memory with one bulk copy
+    uint64_t* zbar = reinterpret_cast<uint64_t*>(V + big_y_floats2(R, m2));
+    const uint32_t zbytes = 16u * (uint32_t)m1 * (uint32_t)m2;
+    if constexpr (ZS) {
+        if (threadIdx.x == 0) {
+            mbar_init(zbar, 1);
+            fence_barrier_init();
+            mbar_arrive_expect_tx(zbar, zbytes);
+            bulk_load(sm, Zp, zbytes, zbar);
+        }
+        __syncthreads();
+    }
+
+    if constexpr (ZS) {
+        if (!wait_parity_bounded(zbar, 0, err)) {
+            // err is set and the output is void; still wait (bounded) for the
+            // copy before the shared memory is rewritten
+            if (threadIdx.x == 0) wait_parity_bounded(zbar, 0, nullptr);
+        }
+        columns_inverse<R, 0, true>(scr, V, ys, sm, H, m1, m2, P, p, tw_h);
+    } else {
+        columns_inverse<R>(scr, V, ys, Zp, H, m1, m2, P, p, tw_h);
+    }
     __syncthreads();
 
     const int g = threadIdx.x / L, t = threadIdx.x % L;
-    float2* S = scr + g * B::GroupScr;  // S[kk][n1], row stride L + G
     const int kk2 = t / G, a = t % G;
     float2 tw1[16], tw2[NK];
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) tw1[kk] = root<1>(tw_w, t * kk, W);
 #pragma unroll
     for (int j = 0; j < NK; ++j) tw2[j] = root<1>(tw_w, 16 * a * cand_k1<L>(j), W);
+    float2* S = scr + g * B::GroupScr;  // S[kk][n1], row stride L + G
     float* yp = y + (size_t)plane * H * W;
 
     constexpr int npairs = R / 2;
@@ -258,12 +337,16 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
 
 template <int W, int R>
 cudaError_t set_attrs() {
-    const int bytes = (int)std::min<size_t>(big_smem_bytes<W, R>(64), 227 * 1024);
-    cudaError_t e = cudaFuncSetAttribute(fwd_big_kernel<W, R>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const int fb = (int)std::min<size_t>(big_smem_bytes<W, R, true>(64), 227 * 1024);
+    const int ib = (int)std::min<size_t>(big_smem_bytes<W, R, false>(64), 227 * 1024);
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd_big_kernel<W, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, fb);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(inv_big_kernel<W, R>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        e = cudaFuncSetAttribute(inv_big_kernel<W, R, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, ib);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(inv_big_kernel<W, R, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, ib);
     return e;
 }
 
@@ -279,15 +362,20 @@ cudaError_t set_attrs_w() {
 template <bool FWD, int W, int R>
 cudaError_t launch(const fno_plan_s& p, const float* x, float2* X, const float2* Z, float* y,
                    cudaStream_t s) {
-    const size_t smem = big_smem_bytes<W, R>(p.m2);
     if (FWD) {
+        const size_t smem = big_smem_bytes<W, R, true>(p.m2);
         const unsigned grid = (unsigned)((size_t)p.B * p.Cin * p.P);
         fwd_big_kernel<W, R><<<grid, kBT, smem, s>>>(x, X, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
-                                                     p.tw_h);
+                                                     p.tw_h, p.err);
     } else {
+        const size_t smem = big_smem_bytes<W, R, false>(p.m2);
         const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.Pi);
-        inv_big_kernel<W, R><<<grid, kBT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w,
-                                                     p.tw_h);
+        if (big_z_staged<W, R>(p.m1, p.m2))
+            inv_big_kernel<W, R, true><<<grid, kBT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.Pi, p.scale,
+                                                               p.tw_w, p.tw_h, p.err);
+        else
+            inv_big_kernel<W, R, false><<<grid, kBT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.Pi,
+                                                                p.scale, p.tw_w, p.tw_h, p.err);
     }
     return cudaGetLastError();
 }
@@ -329,9 +417,10 @@ cudaError_t stages_big_init() {
     return e;
 }
 
-size_t big_smem_bytes_any(int W, int R, int m2) {
+size_t big_smem_bytes_any(int W, int R, int m2, bool fwd) {
     switch (W * 1000 + R) {
-#define CASE(w, r) case w * 1000 + r: return big_smem_bytes<w, r>(m2);
+#define CASE(w, r) \
+    case w * 1000 + r: return fwd ? big_smem_bytes<w, r, true>(m2) : big_smem_bytes<w, r, false>(m2);
         CASE(512, 32) CASE(512, 64) CASE(512, 128) CASE(512, 256)
         CASE(1024, 32) CASE(1024, 64) CASE(1024, 128) CASE(1024, 256)
         CASE(2048, 32) CASE(2048, 64) CASE(2048, 128) CASE(2048, 256)
@@ -339,6 +428,19 @@ size_t big_smem_bytes_any(int W, int R, int m2) {
 #undef CASE
     }
     return (size_t)-1;
+}
+
+bool big_z_staged_any(int W, int R, int m1, int m2) {
+    switch (W * 1000 + R) {
+#define CASE(w, r) \
+    case w * 1000 + r: return big_z_staged<w, r>(m1, m2);
+        CASE(512, 32) CASE(512, 64) CASE(512, 128) CASE(512, 256)
+        CASE(1024, 32) CASE(1024, 64) CASE(1024, 128) CASE(1024, 256)
+        CASE(2048, 32) CASE(2048, 64) CASE(2048, 128) CASE(2048, 256)
+        CASE(4096, 32) CASE(4096, 64) CASE(4096, 128) CASE(4096, 256)
+#undef CASE
+    }
+    return false;
 }
 
 cudaError_t launch_forward_big(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s) {

@@ -500,20 +500,26 @@ bool fused_supported(int W, int H, int m1, int m2, int* R_fwd, int* R_inv) {
     // the column length R: the whole column when it fits (P = 1), else strided
     // row groups h = p + P*q of R rows per CTA (the forward adds its groups into
     // X with atomics; retained frequencies sharing a residue mod R read the
-    // same value, so R need not reach 2*m1).  Measured at 2048 x 2048, m1 = 64:
-    // forward R = 32 / 64 / 128 -> 414 / 299 / 339 us, inverse R = 64 / 128 /
-    // 256 -> 340 / 297 / 425 us.
+    // same value, so R need not reach 2*m1).  Long rows take R = 64 for the
+    // inverse too when the plane's Z can be staged in shared memory.  Measured
+    // at 2048 x 2048, m1 = m2 = 64: forward R = 32 / 64 / 128 -> 379 / 259 /
+    // 318 us; inverse R = 64 / 128 -> 289 / 302 us with Z staged, 336 / 296
+    // without.
     int Rf = H, Ri = H;
     if (H > 256) {
         Rf = 64;
-        Ri = 32;
-        while (Ri < 2 * m1 && Ri < 128) Ri <<= 1;
+        if (W > 256 && big_z_staged_any(W, 64, m1, m2)) {
+            Ri = 64;
+        } else {
+            Ri = 32;
+            while (Ri < 2 * m1 && Ri < 128) Ri <<= 1;
+        }
     }
     if (H <= 256 && H < 2 * m1) return false;
-    const auto smem = [&](int R) {
-        return W <= 256 ? fused_smem_bytes_any(W, R, m2) : big_smem_bytes_any(W, R, m2);
+    const auto smem = [&](int R, bool fwd) {
+        return W <= 256 ? fused_smem_bytes_any(W, R, m2) : big_smem_bytes_any(W, R, m2, fwd);
     };
-    if (smem(Rf) > 227 * 1024 || smem(Ri) > 227 * 1024) return false;
+    if (smem(Rf, true) > 227 * 1024 || smem(Ri, false) > 227 * 1024) return false;
     *R_fwd = Rf;
     *R_inv = Ri;
     return true;

@@ -82,6 +82,18 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes from global memory into shared memory,
+// completing on `bar` (complete_tx).  Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Ask the TMA unit to pull [p, p + bytes) into L2 (no completion to wait for).
 // p and bytes must be multiples of 16.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {

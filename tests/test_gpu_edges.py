@@ -23,7 +23,7 @@ EDGE_SHAPES = [
     (1, 1, 2, 2, 4096, 1, 2049),    # longest row transform, every column kept
     (2, 33, 31, 32, 32, 7, 9),      # channel counts off the tile sizes
     # fused transform path: row groups h = p + P*q with P > 1 (forward R = 64,
-    # inverse R = 32..128 once H > 256), Nyquist, non-square
+    # inverse R = 32..128, or 64 for long rows, once H > 256), Nyquist, non-square
     (2, 3, 4, 512, 64, 16, 9),      # fwd P = 8, inv R = 32, P = 16
     (1, 2, 2, 1024, 128, 64, 65),   # two retained frequencies per forward residue, Nyquist kept
     (2, 4, 4, 64, 256, 32, 129),    # 2*m1 = H, m2 = W/2 + 1
@@ -42,6 +42,7 @@ EDGE_SHAPES = [
     (1, 1, 2, 256, 4096, 32, 17),   # W = 4096, one row group per CTA
     (2, 2, 3, 512, 2048, 128, 5),   # 2*m1 = 256 > both column lengths
     (1, 3, 3, 1024, 2048, 64, 1),   # a single kept column
+    (1, 2, 2, 1024, 512, 64, 64),   # R = 64 = m1: both sides of every residue, Z staged in shared memory
 ]
 
 
