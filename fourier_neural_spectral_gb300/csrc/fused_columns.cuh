@@ -160,30 +160,41 @@ __device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys, 
     for (int c0 = 0; c0 < m2; c0 += CP) {
         const int col = c0 + cs;
         const bool active = col < m2;
-        // the inputs U[16*k1 + kk] for kk = t + Bq*j
-        float2 u[J][Bq];
-        if (active) {
+        // the inputs U[16*k1 + kk] for kk = t + Bq*j; from shared memory all of
+        // them are read before the barrier that frees the scratch
+        const auto gather = [&](float2 (&u)[Bq], int j) {
 #pragma unroll
-            for (int j = 0; j < J; ++j)
+            for (int k1 = 0; k1 < Bq; ++k1)
+                u[k1] = k1_live<R, M1S>(k1)
+                            ? gather_residue<R, ZS>(Zp, 16 * k1 + t + Bq * j, col, H, m1, m2, P, p,
+                                                    cup, tw_h)
+                            : make_float2(0.f, 0.f);
+        };
+        float2 ug[ZS ? J : 1][Bq];
+        if (ZS) {
+            if (active) {
 #pragma unroll
-                for (int k1 = 0; k1 < Bq; ++k1)
-                    u[j][k1] = k1_live<R, M1S>(k1)
-                                   ? gather_residue<R, ZS>(Zp, 16 * k1 + t + Bq * j, col, H, m1,
-                                                           m2, P, p, cup, tw_h)
-                                   : make_float2(0.f, 0.f);
+                for (int j = 0; j < J; ++j) gather(ug[ZS ? j : 0], j);
+            }
+            __syncthreads();
         }
-        if (ZS) __syncthreads();  // Z fully read before the scratch is rewritten
         if (active) {
             // pass 1 (transposed): for kk = t + Bq*j, inverse Bq-point DFT over
             // k1, then times e^{+2 pi i n1 kk / R}
 #pragma unroll
             for (int j = 0; j < J; ++j) {
                 const int kk = t + Bq * j;
-                dft<Bq, 1>(u[j]);
+                float2 u[Bq];
+                if (ZS) {
+#pragma unroll
+                    for (int k1 = 0; k1 < Bq; ++k1) u[k1] = ug[ZS ? j : 0][k1];
+                } else {
+                    gather(u, j);
+                }
+                dft<Bq, 1>(u);
 #pragma unroll
                 for (int n1 = 0; n1 < Bq; ++n1) {
-                    const float2 w =
-                        n1 == 0 ? u[j][n1] : cmul(u[j][n1], root<1>(tw_h, n1 * kk * P, H));
+                    const float2 w = n1 == 0 ? u[n1] : cmul(u[n1], root<1>(tw_h, n1 * kk * P, H));
                     S[n1 * 16 + kk] = w;
                 }
             }

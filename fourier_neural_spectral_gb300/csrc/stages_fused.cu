@@ -35,6 +35,7 @@
 #include "fft_reg.cuh"
 #include "fused_columns.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace fno {
 namespace {
@@ -77,10 +78,19 @@ struct FusedCfg {
 // groups fall on different shared-memory banks.
 __host__ __device__ inline int kept_stride(int m2) { return m2 + ((4 - m2 % 8) + 8) % 8; }
 
+// The inverse of 128- and 256-point rows can bring the plane's Z into shared
+// memory with one bulk copy (fused_z_staged).  Staging the forward's row pairs
+// and the inverse's output rows through shared memory by bulk copies was
+// measured too (128 x 128: no gain; 256 x 256: forward 76 -> 111 us, inverse
+// 87 -> 94 us) and is not used.
+template <int W>
+constexpr bool staged_z() { return W >= 128; }
+
+// Shared memory: scratch | Y or V [R][ys] | one mbarrier (staged Z).
 template <int W, int R>
 size_t fused_smem_bytes(int m2) {
     using C = FusedCfg<W, R>;
-    return sizeof(float2) * ((size_t)C::Scratch + (size_t)R * kept_stride(m2));
+    return sizeof(float2) * ((size_t)C::Scratch + (size_t)R * kept_stride(m2)) + sizeof(uint64_t);
 }
 
 // Mirror partner of bin kk of the 16-point first pass: kk and (16 - kk) mod 16
@@ -343,23 +353,59 @@ fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int
 }
 
 // ---------------------------------------------------------------- inverse ---
-template <int W, int R, int M1S = 0, int M2S = 0>
+// Whether the inverse brings the plane's Z (16*m1*m2 bytes, contiguous) into
+// shared memory with one bulk copy: rows of 128 or 256 points, a single column
+// pass, and Z fitting over the scratch and V (overwritten only after Z is read).
+template <int W, int R>
+bool fused_z_staged(int m1, int m2) {
+    using C = FusedCfg<W, R>;
+    return staged_z<W>() && m2 <= ColCfg<R>::CP &&
+           16ull * m1 * m2 <= sizeof(float2) * ((size_t)C::Scratch + (size_t)R * kept_stride(m2));
+}
+
+// Z staging is compiled where the register budget holds it without spills:
+// the kernels specialised for (m1, m2), or those sized for <= 2 CTAs per SM.
+template <int W, int R, int M2S>
+constexpr bool zs_compiled() {
+    return staged_z<W>() && (M2S > 0 || FusedCfg<W, R>::MinBlocks <= 2);
+}
+
+template <int W, int R, int M1S = 0, int M2S = 0, bool ZS = false>
 __global__ void __launch_bounds__(kFT, (FusedCfg<W, R>::MinBlocks))
 inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m1, int m2,
                  int P, float scale, const float2* __restrict__ tw_w,
-                 const float2* __restrict__ tw_h) {
+                 const float2* __restrict__ tw_h, unsigned* __restrict__ err) {
     using C = FusedCfg<W, R>;
-    extern __shared__ float2 sm[];
+    extern __shared__ __align__(16) float2 sm[];
     float2* scr = sm;
     float2* V = sm + C::Scratch;  // [R][ys]
     const int ys = kept_stride(M2S ? M2S : m2);
+    uint64_t* zbar = reinterpret_cast<uint64_t*>(V + R * ys);
     const int plane = blockIdx.x / P;
     const int p = blockIdx.x - plane * P;
     const int R2 = 2 * m1;
     const float2* Zp = Z + (size_t)plane * R2 * m2;
 
     // ---- columns: retained rows of Z -> V[q][col], q in [0, R) ----------
-    columns_inverse<R, M1S>(scr, V, ys, Zp, H, m1, m2, P, p, tw_h);
+    // ZS (fused_z_staged): the plane's Z comes into shared memory first
+    if constexpr (ZS) {
+        const uint32_t zbytes = 16u * (uint32_t)(M1S ? M1S : m1) * (uint32_t)(M2S ? M2S : m2);
+        if (threadIdx.x == 0) {
+            mbar_init(zbar, 1);
+            fence_barrier_init();
+            mbar_arrive_expect_tx(zbar, zbytes);
+            bulk_load(sm, Zp, zbytes, zbar);
+        }
+        __syncthreads();
+        if (!wait_parity_bounded(zbar, 0, err)) {
+            // err is set and the output is void; still wait (bounded) for the
+            // copy before the shared memory is rewritten
+            if (threadIdx.x == 0) wait_parity_bounded(zbar, 0, nullptr);
+        }
+        columns_inverse<R, M1S, true>(scr, V, ys, sm, H, m1, m2, P, p, tw_h);
+    } else {
+        columns_inverse<R, M1S>(scr, V, ys, Zp, H, m1, m2, P, p, tw_h);
+    }
     __syncthreads();
 
     // ---- rows: pairs of V rows -> two real output rows ------------------
@@ -402,6 +448,9 @@ cudaError_t set_attrs() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(inv_fused_kernel<W, R>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && zs_compiled<W, R, 0>())
+        e = cudaFuncSetAttribute(inv_fused_kernel<W, R, 0, 0, zs_compiled<W, R, 0>()>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if constexpr (has_static<W, R>()) {
         const int sb = (int)std::min<size_t>(fused_smem_bytes<W, R>(W / 4), 227 * 1024);
         if (e == cudaSuccess)
@@ -409,6 +458,9 @@ cudaError_t set_attrs() {
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(inv_fused_kernel<W, R, W / 4, W / 4>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
+        if (e == cudaSuccess && zs_compiled<W, R, W / 4>())
+            e = cudaFuncSetAttribute(inv_fused_kernel<W, R, W / 4, W / 4, zs_compiled<W, R, W / 4>()>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
     }
     return e;
@@ -439,20 +491,25 @@ cudaError_t launch_fwd(const fno_plan_s& p, const float* x, float2* X, cudaStrea
     return cudaGetLastError();
 }
 
-template <int W, int R>
-cudaError_t launch_inv(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s) {
+template <int W, int R, int M1S, int M2S>
+cudaError_t launch_inv_zs(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s) {
     const size_t smem = fused_smem_bytes<W, R>(p.m2);
     const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.Pi);
-    if constexpr (has_static<W, R>()) {
-        if (p.m1 == W / 4 && p.m2 == W / 4) {
-            inv_fused_kernel<W, R, W / 4, W / 4><<<grid, kFT, smem, s>>>(
-                Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h);
-            return cudaGetLastError();
-        }
-    }
-    inv_fused_kernel<W, R><<<grid, kFT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w,
-                                                   p.tw_h);
+    if (zs_compiled<W, R, M2S>() && fused_z_staged<W, R>(p.m1, p.m2))
+        inv_fused_kernel<W, R, M1S, M2S, zs_compiled<W, R, M2S>()><<<grid, kFT, smem, s>>>(
+            Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
+    else
+        inv_fused_kernel<W, R, M1S, M2S, false><<<grid, kFT, smem, s>>>(
+            Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
     return cudaGetLastError();
+}
+
+template <int W, int R>
+cudaError_t launch_inv(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s) {
+    if constexpr (has_static<W, R>()) {
+        if (p.m1 == W / 4 && p.m2 == W / 4) return launch_inv_zs<W, R, W / 4, W / 4>(p, Z, y, s);
+    }
+    return launch_inv_zs<W, R, 0, 0>(p, Z, y, s);
 }
 
 template <bool FWD, int W>
