@@ -94,6 +94,7 @@ void set_kernel(fno_plan_s* p, int k, const char* name, size_t bytes, size_t flo
 
 const char* mix_name(const fno_plan_s* p) {
     if (p->mix_path == 2) return p->tc_split == 3 ? "mix_tc_3xtf32" : "mix_tc_tf32";
+    if (p->mix_path == 3) return "mix_wide";
     return p->mix_path == 1 ? "mix_tma" : "mix_fma";
 }
 
@@ -139,6 +140,7 @@ cudaError_t run_inverse(const fno_plan_s& p, const float2* Z, float* y, float2* 
 cudaError_t run_mix(const fno_plan_s& p, const float2* X, const float2* w, float2* Z, cudaStream_t s,
                     fno_launch_ctx* ctx) {
     if (p.mix_path == 2) return launch_mix_tc(p, X, w, Z, p.tc_split, s, ctx);
+    if (p.mix_path == 3) return launch_mix_wide(p, X, w, Z, s, ctx);
     return p.mix_path == 1 ? launch_mix_tma(p, X, w, Z, s, ctx) : launch_mix_modes(p, X, w, Z, s, ctx);
 }
 
@@ -183,6 +185,7 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
         if (g_init_err == cudaSuccess) g_init_err = stages_big_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_tma_init();
+        if (g_init_err == cudaSuccess) g_init_err = mix_wide_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_tc_init();
     });
     if (g_init_err != cudaSuccess) return FNO_ERR_CUDA;
@@ -202,6 +205,10 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     p->Ri = p->path == 1 ? Ri : H;
     p->Pi = H / p->Ri;
     p->mix_path = mix_tma_supported(B, Cin, Cout, p->nm) ? 1 : 0;
+    // 32-mode blocks move w and X as 256-byte rows (measured faster than the
+    // 4-mode mix_tma at every workload: 128x128 44.7 -> 38.2 us, 256x256 222 ->
+    // 207 us, 2048x2048 25.2 -> 19.8 us)
+    if (mix_wide_supported(B, Cin, Cout, p->nm)) p->mix_path = 3;
     p->tc_split = prec == FNO_PREC_3XTF32 ? 3 : 1;
     // tensor cores for the contraction only where it is a real dense product
     if (prec != FNO_PREC_FP32 && Cin >= 32 && Cout >= 32 &&

@@ -36,6 +36,10 @@ EDGE_SHAPES = [
     (3, 33, 40, 32, 32, 3, 5),      # B < batch tile, Cin % IC != 0, Cout % 32 != 0, NM % 4 == 2
     (5, 16, 96, 64, 32, 4, 4),      # B = 5 -> batch tile 8 split over two warp groups
     (20, 32, 32, 32, 32, 2, 3),     # B > 16: two batch tiles
+    # 32-mode contraction blocks: ragged mode block, channel and batch tiles
+    (5, 19, 13, 64, 64, 9, 11),     # nm = 198, Cout % 8 != 0, B = 5, Cin % IC != 0
+    (20, 7, 9, 32, 64, 4, 9),       # B > 16: two batch tiles, nm = 72
+    (1, 3, 2, 64, 32, 8, 2),        # B = 1, nm = 32 exactly
     # long rows (three-level row transform, shuffle reduce-scatter)
     (2, 3, 4, 64, 512, 16, 33),     # W = 512
     (1, 2, 2, 32, 1024, 8, 64),     # W = 1024, the largest supported m2
