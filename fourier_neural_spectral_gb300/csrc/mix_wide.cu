@@ -27,8 +27,11 @@ namespace {
 constexpr int kModes = 32;  // modes per CTA (one per lane)
 constexpr int kOCB = 8;     // output channels per CTA
 constexpr int kJO = 4;      // output channels per thread (two warp halves)
-constexpr int kNST = 4;     // ring depth
-constexpr size_t kStageTarget = 12 * 1024;
+constexpr int kNST = 2;     // ring depth
+// Stage size and ring depth, measured (128x128 / 256x256 / 2048x2048 contraction, us):
+// 4 x 12 KB 37.6 / 206 / 19.9, 3 x 18 KB 36.1 / 208 / 18.6, 2 x 24 KB 35.3 / 197 / 18.8,
+// 6 x 8 KB 45.8 / 201 / 20.7: fewer, larger stages (fewer CTA barriers) win.
+constexpr size_t kStageTarget = 24 * 1024;
 
 struct MixWideCfg {
     int BT, JB, NBW, IC;
