@@ -12,9 +12,11 @@
 //   * warp (oh, bh) accumulates 4 output channels x JB batch rows for its lane's
 //     mode in registers; every shared-memory read is a lane-contiguous 8-byte
 //     load (conflict-free), and each thread does 4*JB complex MACs per 4 + JB
-//     loads.
-// Every wait is bounded (see tma.cuh); on a timeout the CTA drains its copies
-// and returns with the error word set.
+//     loads;
+//   * a producer warp refills each stage once all consumer warps have released
+//     it (one "full" and one "empty" mbarrier per stage, no CTA-wide barrier).
+// Every wait is bounded (see tma.cuh); after a timeout the error word is set,
+// the producer waits (bounded) for its copies in flight and the CTA returns.
 #include <algorithm>
 
 #include "common.cuh"
@@ -30,84 +32,114 @@ constexpr int kJO = 4;      // output channels per thread (two warp halves)
 constexpr int kNST = 2;     // ring depth
 // Stage size and ring depth, measured (128x128 / 256x256 / 2048x2048 contraction, us):
 // 4 x 12 KB 37.6 / 206 / 19.9, 3 x 18 KB 36.1 / 208 / 18.6, 2 x 24 KB 35.3 / 197 / 18.8,
-// 6 x 8 KB 45.8 / 201 / 20.7: fewer, larger stages (fewer CTA barriers) win.
+// 6 x 8 KB 45.8 / 201 / 20.7: fewer, larger stages win.
 constexpr size_t kStageTarget = 24 * 1024;
+constexpr size_t kRowBytes = kModes * sizeof(float2);  // 256
 
-struct MixWideCfg {
-    int BT, JB, NBW, IC;
-    size_t stage_bytes, smem;
+// Per batch tile BT (a power of two <= 16): batch rows per thread, consumer
+// warps along the batch, and input channels per stage.
+template <int BT>
+struct WideTile {
+    static constexpr int JB = BT >= 2 ? BT / 2 : 1;
+    static constexpr int NBW = BT / JB;
+    static constexpr int IC = (int)(kStageTarget / (kRowBytes * (kOCB + BT)));
+    static constexpr int Consumers = 2 * NBW;  // warps
+    static constexpr int Threads = 32 * (Consumers + 1);  // + one producer warp
+    static constexpr uint32_t WBytes = (uint32_t)(kRowBytes * kOCB * IC);
+    static constexpr uint32_t StageBytes = (uint32_t)(kRowBytes * IC * (kOCB + BT));
+    static constexpr size_t Smem = 128 + (size_t)kNST * StageBytes;
 };
 
-MixWideCfg mix_wide_cfg(int B, int Cin) {
-    MixWideCfg c;
+int wide_bt(int B) {
     int bt = 1;
     while (bt < B && bt < 16) bt <<= 1;
-    c.BT = bt;
-    c.JB = std::max(1, bt / 2);
-    c.NBW = bt / c.JB;
-    const size_t row = (size_t)kModes * sizeof(float2);  // 256 bytes
-    c.IC = (int)std::max<size_t>(1, std::min<size_t>(Cin, kStageTarget / (row * (kOCB + bt))));
-    c.stage_bytes = row * c.IC * (kOCB + bt);
-    c.smem = 128 + (size_t)kNST * c.stage_bytes;
-    return c;
+    return bt;
 }
 
-// Threads: 64 * NBW.  Warp w: oh = w & 1 (output channels o0 + 4*oh .. + 3),
-// bh = w >> 1 (batch rows b0 + JB*bh .. + JB - 1); lane = mode m0 + lane.
-template <int JB>
-__global__ void __launch_bounds__(128)
+size_t wide_smem(int bt) {
+    switch (bt) {
+        case 1: return WideTile<1>::Smem;
+        case 2: return WideTile<2>::Smem;
+        case 4: return WideTile<4>::Smem;
+        case 8: return WideTile<8>::Smem;
+        default: return WideTile<16>::Smem;
+    }
+}
+
+// Warps 0 .. Consumers-1 compute: warp w takes output channels o0 + 4*(w & 1)
+// .. + 3 and batch rows b0 + JB*(w >> 1) .. + JB - 1 of its lane's mode
+// m0 + lane.  The last warp is the producer: its lane 0 refills a stage with
+// TMA once every consumer warp has released it (per-stage "empty" mbarrier),
+// so consumer warps never wait for one another.  Input channels past Cin in
+// the last stage arrive as zeros (TMA fill) and add nothing.
+template <int BT>
+__global__ void __launch_bounds__(WideTile<BT>::Threads, 4)
 mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                float2* __restrict__ Z, int B, int Cin, int Cout, int NM, int IC, int BT,
+                float2* __restrict__ Z, int B, int Cin, int Cout, int NM,
                 unsigned* __restrict__ err) {
+    using T = WideTile<BT>;
+    constexpr int JB = T::JB, IC = T::IC;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kNST;
     unsigned char* stages = smem + 128;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int oh = warp & 1, bh = warp >> 1;
     const int m0 = blockIdx.x * kModes, o0 = blockIdx.y * kOCB, b0 = blockIdx.z * BT;
     const int nch = (Cin + IC - 1) / IC;
-    const uint32_t w_bytes = (uint32_t)(kModes * sizeof(float2)) * kOCB * IC;
-    const uint32_t stage_bytes = w_bytes + (uint32_t)(kModes * sizeof(float2)) * IC * BT;
 
     if (tid == 0) {
-        prefetch_tensormap(&tmW);
-        prefetch_tensormap(&tmX);
-        for (int s = 0; s < kNST; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < kNST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], T::Consumers);
+        }
         fence_barrier_init();
     }
     __syncthreads();
-    int issued = 0;  // stages handed to the TMA unit (thread 0 only)
-    if (tid == 0) {
-        for (; issued < kNST && issued < nch; ++issued) {
-            unsigned char* st = stages + (size_t)issued * stage_bytes;
-            mbar_arrive_expect_tx(&bars[issued], stage_bytes);
-            tma_load_3d(st, &tmW, 2 * m0, o0, issued * IC, &bars[issued]);
-            tma_load_3d(st + w_bytes, &tmX, 2 * m0, issued * IC, b0, &bars[issued]);
+
+    if (warp == T::Consumers) {
+        // ---- producer --------------------------------------------------
+        if (lane == 0) {
+            prefetch_tensormap(&tmW);
+            prefetch_tensormap(&tmX);
+            int issued = 0;
+            for (int c = 0; c < nch; ++c) {
+                const int s = c % kNST;
+                // stage s last held chunk c - kNST: wait until every consumer let it go
+                if (c >= kNST &&
+                    !wait_parity_bounded(&empty[s], (uint32_t)((c / kNST - 1) & 1), err))
+                    break;
+                unsigned char* st = stages + (size_t)s * T::StageBytes;
+                mbar_arrive_expect_tx(&full[s], T::StageBytes);
+                tma_load_3d(st, &tmW, 2 * m0, o0, c * IC, &full[s]);
+                tma_load_3d(st + T::WBytes, &tmX, 2 * m0, c * IC, b0, &full[s]);
+                issued = c + 1;
+            }
+            // no copy may be in flight when the CTA leaves: the last kNST issued
+            // chunks are the only ones not known to have landed (bounded waits)
+            for (int c = issued > kNST ? issued - kNST : 0; c < issued; ++c)
+                wait_parity_bounded(&full[c % kNST], (uint32_t)((c / kNST) & 1), nullptr);
         }
+        return;
     }
 
+    // ---- consumers ------------------------------------------------------
+    const int oh = warp & 1, bh = warp >> 1;
     float2 acc[kJO][JB];
 #pragma unroll
     for (int j = 0; j < kJO; ++j)
 #pragma unroll
         for (int bb = 0; bb < JB; ++bb) acc[j][bb] = make_float2(0.f, 0.f);
 
-    int consumed = 0;
-    bool timed_out = false;
     for (int c = 0; c < nch; ++c) {
         const int s = c % kNST;
-        const bool ok = wait_parity_bounded(&bars[s], (uint32_t)((c / kNST) & 1), err);
-        if (__syncthreads_or(!ok)) {
-            timed_out = true;
-            break;
-        }
-        consumed = c + 1;
-        const unsigned char* st = stages + (size_t)s * stage_bytes;
+        if (!wait_parity_bounded(&full[s], (uint32_t)((c / kNST) & 1), err)) return;
+        const unsigned char* st = stages + (size_t)s * T::StageBytes;
         // w stage [IC][kOCB][32 modes], X stage [BT][IC][32 modes]
         const float2* Ws = reinterpret_cast<const float2*>(st) + (oh * kJO) * kModes + lane;
-        const float2* Xs = reinterpret_cast<const float2*>(st + w_bytes) + (bh * JB) * IC * kModes + lane;
-        const int ni = min(IC, Cin - c * IC);
-        for (int ii = 0; ii < ni; ++ii) {
+        const float2* Xs =
+            reinterpret_cast<const float2*>(st + T::WBytes) + (bh * JB) * IC * kModes + lane;
+#pragma unroll
+        for (int ii = 0; ii < IC; ++ii) {
             float2 wv[kJO], xv[JB];
 #pragma unroll
             for (int j = 0; j < kJO; ++j) wv[j] = Ws[(ii * kOCB + j) * kModes];
@@ -118,22 +150,8 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 #pragma unroll
                 for (int bb = 0; bb < JB; ++bb) cmac(acc[j][bb], xv[bb], wv[j]);
         }
-        __syncthreads();  // every thread is done with stage s
-        if (tid == 0 && issued < nch) {
-            unsigned char* st2 = stages + (size_t)s * stage_bytes;
-            mbar_arrive_expect_tx(&bars[s], stage_bytes);
-            tma_load_3d(st2, &tmW, 2 * m0, o0, issued * IC, &bars[s]);
-            tma_load_3d(st2 + w_bytes, &tmX, 2 * m0, issued * IC, b0, &bars[s]);
-            ++issued;
-        }
-    }
-    if (timed_out) {
-        // drain: wait (bounded) for every copy still in flight, then leave
-        if (tid == 0)
-            for (int c = consumed; c < issued; ++c)
-                wait_parity_bounded(&bars[c % kNST], (uint32_t)((c / kNST) & 1), err);
-        __syncthreads();
-        return;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
     }
 
     const int m = m0 + lane;
@@ -151,10 +169,18 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     }
 }
 
-template <int JB>
+template <int BT>
 cudaError_t set_attr() {
-    return cudaFuncSetAttribute(mix_wide_kernel<JB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                227 * 1024);
+    return cudaFuncSetAttribute(mix_wide_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)WideTile<BT>::Smem);
+}
+
+template <int BT>
+void launch_bt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, const fno_plan_s& p,
+               cudaStream_t s) {
+    const dim3 grid((p.nm + kModes - 1) / kModes, (p.Cout + kOCB - 1) / kOCB, (p.B + BT - 1) / BT);
+    mix_wide_kernel<BT><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
+        mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.err);
 }
 
 // 3D tensor map over a complex64 array [d2][d1][NM] viewed as floats: dims
@@ -184,42 +210,37 @@ cudaError_t mix_wide_init() {
     if (e == cudaSuccess) e = set_attr<2>();
     if (e == cudaSuccess) e = set_attr<4>();
     if (e == cudaSuccess) e = set_attr<8>();
+    if (e == cudaSuccess) e = set_attr<16>();
     return e;
 }
 
 bool mix_wide_supported(int B, int Cin, int Cout, int nm) {
     (void)Cout;
     if (nm < kModes || (nm & 1) || B < 1 || Cin < 1) return false;
-    return mix_wide_cfg(B, Cin).smem <= 227 * 1024;
+    return wide_smem(wide_bt(B)) <= 227 * 1024;
 }
 
 cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                             cudaStream_t s, fno_launch_ctx* ctx) {
-    const MixWideCfg c = mix_wide_cfg(p.B, p.Cin);
+    const int bt = wide_bt(p.B);
+    int ic = 0;
+    switch (bt) {
+        case 1: ic = WideTile<1>::IC; break;
+        case 2: ic = WideTile<2>::IC; break;
+        case 4: ic = WideTile<4>::IC; break;
+        case 8: ic = WideTile<8>::IC; break;
+        default: ic = WideTile<16>::IC; break;
+    }
     CUtensorMap mw, mx;
-    if (!encode_wide_map(&mw, w, p.nm, p.Cout, p.Cin, kOCB, c.IC) ||
-        !encode_wide_map(&mx, X, p.nm, p.Cin, p.B, c.IC, c.BT))
+    if (!encode_wide_map(&mw, w, p.nm, p.Cout, p.Cin, kOCB, ic) ||
+        !encode_wide_map(&mx, X, p.nm, p.Cin, p.B, ic, bt))
         return cudaErrorInvalidValue;
-    const dim3 grid((p.nm + kModes - 1) / kModes, (p.Cout + kOCB - 1) / kOCB,
-                    (p.B + c.BT - 1) / c.BT);
-    const int threads = 64 * c.NBW;
-    switch (c.JB) {
-        case 1:
-            mix_wide_kernel<1><<<grid, threads, c.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm,
-                                                             c.IC, c.BT, p.err);
-            break;
-        case 2:
-            mix_wide_kernel<2><<<grid, threads, c.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm,
-                                                             c.IC, c.BT, p.err);
-            break;
-        case 4:
-            mix_wide_kernel<4><<<grid, threads, c.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm,
-                                                             c.IC, c.BT, p.err);
-            break;
-        default:
-            mix_wide_kernel<8><<<grid, threads, c.smem, s>>>(mw, mx, Z, p.B, p.Cin, p.Cout, p.nm,
-                                                             c.IC, c.BT, p.err);
-            break;
+    switch (bt) {
+        case 1: launch_bt<1>(mw, mx, Z, p, s); break;
+        case 2: launch_bt<2>(mw, mx, Z, p, s); break;
+        case 4: launch_bt<4>(mw, mx, Z, p, s); break;
+        case 8: launch_bt<8>(mw, mx, Z, p, s); break;
+        default: launch_bt<16>(mw, mx, Z, p, s); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
