@@ -57,8 +57,15 @@ def _load():
         lib.oracle_inverse_modes.argtypes = [dp, i, i, i, i, i, i, dp]
         lib.oracle_inverse_modes_at.argtypes = [dp, i, i, i, i, i, i, ip, i, dp]
         lib.oracle_spectral_conv2d.argtypes = [dp, dp, i, i, i, i, i, i, i, dp]
+        lib.oracle_backward_modes.argtypes = [dp, i, i, i, i, i, i, dp]
+        lib.oracle_mix_adjoint.argtypes = [dp, dp, i, i, i, i, dp]
+        lib.oracle_backward_input.argtypes = [dp, i, i, i, i, i, i, dp]
+        lib.oracle_weight_grad.argtypes = [dp, dp, i, i, i, i, dp]
+        lib.oracle_spectral_conv2d_backward.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, dp, dp]
         for f in (lib.oracle_forward_modes, lib.oracle_mix_modes, lib.oracle_inverse_modes,
-                  lib.oracle_inverse_modes_at, lib.oracle_spectral_conv2d):
+                  lib.oracle_inverse_modes_at, lib.oracle_spectral_conv2d,
+                  lib.oracle_backward_modes, lib.oracle_mix_adjoint, lib.oracle_backward_input,
+                  lib.oracle_weight_grad, lib.oracle_spectral_conv2d_backward):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -148,6 +155,74 @@ def spectral_conv2d(x, w, m1: int, m2: int) -> np.ndarray:
     _check(_load().oracle_spectral_conv2d(_dptr(x), _dptr(w.view(np.float64)), B, Cin, Cout,
                                           H, W, m1, m2, _dptr(y)), "spectral_conv2d")
     return y
+
+
+def backward_modes(g, m1: int, m2: int) -> np.ndarray:
+    """dL/dZ = c(k2) * orthonormal truncated DFT of g = dL/dy (c = 1 at k2 = 0 and
+    k2 = W/2, else 2)."""
+    g = _real(g)
+    B, C, H, W = g.shape
+    G = np.zeros((B, C, 2 * m1, m2), dtype=np.complex128)
+    _check(_load().oracle_backward_modes(_dptr(g), B, C, H, W, m1, m2,
+                                         _dptr(G.view(np.float64))), "backward_modes")
+    return G
+
+
+def mix_adjoint(G, w) -> np.ndarray:
+    """GX[b,i,m] = sum_o G[b,o,m] conj(w[i,o,m])."""
+    G = _cplx(G)
+    w = _cplx(w)
+    B, Cout = G.shape[:2]
+    Cin, Cout2 = w.shape[:2]
+    assert Cout == Cout2 and G.shape[2:] == w.shape[2:]
+    nm = int(np.prod(G.shape[2:]))
+    GX = np.zeros((B, Cin) + G.shape[2:], dtype=np.complex128)
+    _check(_load().oracle_mix_adjoint(_dptr(G.view(np.float64)), _dptr(w.view(np.float64)),
+                                      B, Cin, Cout, nm, _dptr(GX.view(np.float64))),
+           "mix_adjoint")
+    return GX
+
+
+def backward_input(GX, H: int, W: int) -> np.ndarray:
+    """gx = transpose of the truncated forward DFT applied to GX."""
+    GX = _cplx(GX)
+    B, C, R, m2 = GX.shape
+    gx = np.zeros((B, C, H, W), dtype=np.float64)
+    _check(_load().oracle_backward_input(_dptr(GX.view(np.float64)), B, C, H, W, R // 2, m2,
+                                         _dptr(gx)), "backward_input")
+    return gx
+
+
+def weight_grad(X, G) -> np.ndarray:
+    """gw[i,o,m] = sum_b conj(X[b,i,m]) G[b,o,m]."""
+    X = _cplx(X)
+    G = _cplx(G)
+    B, Cin = X.shape[:2]
+    B2, Cout = G.shape[:2]
+    assert B == B2 and X.shape[2:] == G.shape[2:]
+    nm = int(np.prod(X.shape[2:]))
+    gw = np.zeros((Cin, Cout) + X.shape[2:], dtype=np.complex128)
+    _check(_load().oracle_weight_grad(_dptr(X.view(np.float64)), _dptr(G.view(np.float64)),
+                                      B, Cin, Cout, nm, _dptr(gw.view(np.float64))),
+           "weight_grad")
+    return gw
+
+
+def spectral_conv2d_backward(x, w, g, m1: int, m2: int):
+    """(gx, gw): gradients of a real loss with dL/dy = g, in double.  The
+    complex gradient is dL/dRe(w) + i dL/dIm(w)."""
+    x = _real(x)
+    g = _real(g)
+    w = _cplx(w)
+    B, Cin, H, W = x.shape
+    Cout = w.shape[1]
+    assert w.shape == (Cin, Cout, 2 * m1, m2) and g.shape == (B, Cout, H, W)
+    gx = np.zeros((B, Cin, H, W), dtype=np.float64)
+    gw = np.zeros((Cin, Cout, 2 * m1, m2), dtype=np.complex128)
+    _check(_load().oracle_spectral_conv2d_backward(
+        _dptr(x), _dptr(w.view(np.float64)), _dptr(g), B, Cin, Cout, H, W, m1, m2, _dptr(gx),
+        _dptr(gw.view(np.float64))), "spectral_conv2d_backward")
+    return gx, gw
 
 
 def forward_modes_parallel(x, m1: int, m2: int, threads: int | None = None) -> np.ndarray:

@@ -40,6 +40,19 @@
 //   Z : double [B][Cout][2*m1][m2][2]
 //   y : double [B][Cout][H][W]
 //
+// Backward (gradients of a real loss L given g = dL/dy, with the complex
+// gradient convention dL/dRe(z) + i dL/dIm(z)), derived by differentiating the
+// sums above:
+//   G[b,o,k1,k2]  = c(k2) / sqrt(HW) * sum_{h,w} g[b,o,h,w] exp(-2 pi i (k1 h/H + k2 w/W))
+//                   (c = 1 for k2 = 0 and k2 = W/2, else 2: the weights of the
+//                   complex-to-real step)
+//   GX[b,i,k1,k2] = sum_o G[b,o,k1,k2] * conj(W[i,o,r(k1),k2])
+//   gx[b,i,h,w]   = 1/sqrt(HW) * Re sum_{k1 in R1, k2 in R2} GX[b,i,k1,k2]
+//                   * exp(+2 pi i (k1 h/H + k2 w/W))
+//   gW[i,o,r,k2]  = sum_b conj(X[b,i,r,k2]) * G[b,o,r,k2]
+// Pinned in tests/test_oracle.py by the adjoint identity <J x, g> = <x, gx>,
+// the weight identity <y(x, v), g> = Re sum conj(gW) v, and finite differences.
+//
 // Return value of every entry point: 0 on success, -1 on an invalid argument.
 
 #include <cmath>
@@ -246,6 +259,130 @@ int oracle_inverse_modes_at(const double* Z, int B, int C, int H, int W, int m1,
         out[s] = scale * acc;
     }
     return 0;
+}
+
+// dL/dZ from g = dL/dy: c(k2) times the orthonormal truncated forward DFT of g.
+int oracle_backward_modes(const double* g, int B, int C, int H, int W, int m1, int m2,
+                          double* G) {
+    int rc = oracle_forward_modes(g, B, C, H, W, m1, m2, G);
+    if (rc) return rc;
+    const long long R = 2LL * m1;
+    for (long long p = 0; p < (long long)B * C; ++p)
+        for (long long r = 0; r < R; ++r)
+            for (long long k2 = 0; k2 < m2; ++k2) {
+                const bool self_mirror = (k2 == 0) || (2LL * k2 == W);
+                const double c = self_mirror ? 1.0 : 2.0;
+                double* v = G + 2 * ((p * R + r) * m2 + k2);
+                v[0] *= c;
+                v[1] *= c;
+            }
+    return 0;
+}
+
+// GX[b,i,m] = sum_o G[b,o,m] * conj(w[i,o,m]).
+int oracle_mix_adjoint(const double* G, const double* w, int B, int Cin, int Cout, int nmodes,
+                       double* GX) {
+    if (!G || !w || !GX || B <= 0 || Cin <= 0 || Cout <= 0 || nmodes <= 0) return -1;
+    for (long long b = 0; b < B; ++b) {
+        for (long long i = 0; i < Cin; ++i) {
+            for (long long m = 0; m < nmodes; ++m) {
+                double re = 0.0, im = 0.0;
+                for (long long o = 0; o < Cout; ++o) {
+                    const double* gv = G + 2 * ((b * Cout + o) * nmodes + m);
+                    const double* wv = w + 2 * ((i * Cout + o) * nmodes + m);
+                    // (a + bi) * (c - di) = (ac + bd) + (bc - ad) i
+                    re += gv[0] * wv[0] + gv[1] * wv[1];
+                    im += gv[1] * wv[0] - gv[0] * wv[1];
+                }
+                GX[2 * ((b * Cin + i) * nmodes + m)] = re;
+                GX[2 * ((b * Cin + i) * nmodes + m) + 1] = im;
+            }
+        }
+    }
+    return 0;
+}
+
+// gx = 1/sqrt(HW) * Re sum over the retained bins of GX * exp(+2 pi i (...)),
+// every retained bin with weight 1 (the transpose of the truncated forward DFT).
+int oracle_backward_input(const double* GX, int B, int C, int H, int W, int m1, int m2,
+                          double* gx) {
+    if (!GX || !gx || !shape_ok(B, C, H, W, m1, m2)) return -1;
+    const std::vector<double> tw_w = root_table(W, +1);
+    const std::vector<double> tw_h = root_table(H, +1);
+    const double scale = 1.0 / std::sqrt((double)H * (double)W);
+    const int R = 2 * m1;
+    std::vector<double> V(2 * (size_t)H * m2);
+    for (long long p = 0; p < (long long)B * C; ++p) {
+        const double* Gp = GX + p * (long long)R * m2 * 2;
+        // V[h][k2] = sum_r GX[r][k2] * exp(+2*pi*i*k1(r)*h/H)
+        for (int h = 0; h < H; ++h) {
+            for (int k2 = 0; k2 < m2; ++k2) {
+                double re = 0.0, im = 0.0;
+                for (int r = 0; r < R; ++r) {
+                    long long j = red(row_of(r, H, m1), h, H);
+                    double a = Gp[2 * ((size_t)r * m2 + k2)];
+                    double b = Gp[2 * ((size_t)r * m2 + k2) + 1];
+                    re += a * tw_h[2 * j] - b * tw_h[2 * j + 1];
+                    im += a * tw_h[2 * j + 1] + b * tw_h[2 * j];
+                }
+                V[2 * ((size_t)h * m2 + k2)] = re;
+                V[2 * ((size_t)h * m2 + k2) + 1] = im;
+            }
+        }
+        // gx[h][w] = scale * sum_k2 Re(V[h][k2] * exp(+2*pi*i*k2*w/W))
+        double* gp = gx + p * (long long)H * W;
+        for (int h = 0; h < H; ++h) {
+            for (int w = 0; w < W; ++w) {
+                double acc = 0.0;
+                for (int k2 = 0; k2 < m2; ++k2) {
+                    long long j = red(k2, w, W);
+                    acc += V[2 * ((size_t)h * m2 + k2)] * tw_w[2 * j] -
+                           V[2 * ((size_t)h * m2 + k2) + 1] * tw_w[2 * j + 1];
+                }
+                gp[(size_t)h * W + w] = scale * acc;
+            }
+        }
+    }
+    return 0;
+}
+
+// gw[i,o,m] = sum_b conj(X[b,i,m]) * G[b,o,m].
+int oracle_weight_grad(const double* X, const double* G, int B, int Cin, int Cout, int nmodes,
+                       double* gw) {
+    if (!X || !G || !gw || B <= 0 || Cin <= 0 || Cout <= 0 || nmodes <= 0) return -1;
+    for (long long i = 0; i < Cin; ++i) {
+        for (long long o = 0; o < Cout; ++o) {
+            for (long long m = 0; m < nmodes; ++m) {
+                double re = 0.0, im = 0.0;
+                for (long long b = 0; b < B; ++b) {
+                    const double* xv = X + 2 * ((b * Cin + i) * nmodes + m);
+                    const double* gv = G + 2 * ((b * Cout + o) * nmodes + m);
+                    // (a - bi) * (c + di) = (ac + bd) + (ad - bc) i
+                    re += xv[0] * gv[0] + xv[1] * gv[1];
+                    im += xv[0] * gv[1] - xv[1] * gv[0];
+                }
+                gw[2 * ((i * Cout + o) * nmodes + m)] = re;
+                gw[2 * ((i * Cout + o) * nmodes + m) + 1] = im;
+            }
+        }
+    }
+    return 0;
+}
+
+// The whole backward: gx and gw from x, w and g = dL/dy.
+int oracle_spectral_conv2d_backward(const double* x, const double* w, const double* g, int B,
+                                    int Cin, int Cout, int H, int W, int m1, int m2,
+                                    double* gx, double* gw) {
+    if (!x || !w || !g || !gx || !gw || Cout <= 0 || !shape_ok(B, Cin, H, W, m1, m2)) return -1;
+    const long long nm = 2LL * m1 * m2;
+    std::vector<double> X(2 * (size_t)B * Cin * nm), G(2 * (size_t)B * Cout * nm),
+        GX(2 * (size_t)B * Cin * nm);
+    int rc = oracle_forward_modes(x, B, Cin, H, W, m1, m2, X.data());
+    if (!rc) rc = oracle_backward_modes(g, B, Cout, H, W, m1, m2, G.data());
+    if (!rc) rc = oracle_mix_adjoint(G.data(), w, B, Cin, Cout, (int)nm, GX.data());
+    if (!rc) rc = oracle_backward_input(GX.data(), B, Cin, H, W, m1, m2, gx);
+    if (!rc) rc = oracle_weight_grad(X.data(), G.data(), B, Cin, Cout, (int)nm, gw);
+    return rc;
 }
 
 // The whole layer: inverse(mix(forward(x), w)).

@@ -265,3 +265,89 @@ def test_invalid_shapes_rejected(args):
             oracle.forward_modes(np.zeros((0, C, H, W)), m1, m2)
         else:
             oracle.forward_modes(x, m1, m2)
+
+
+# --------------------------------------------------------------- backward ---
+# The gradients of L = <y, g> for g = dL/dy, with the complex convention
+# dL/dRe(w) + i dL/dIm(w).  Pinned against the (already pinned) forward by
+# identities that hold for any correct gradient of a linear map, and by finite
+# differences; a wrong conjugation, a missing c(k2) weight, a transposed
+# weight or a dropped Nyquist/DC term breaks one of them.
+
+BACKWARD_SHAPES = [
+    # B, Cin, Cout, H, W, m1, m2
+    (2, 3, 2, 8, 8, 2, 3),       # interior columns only
+    (1, 2, 3, 8, 8, 4, 5),       # 2*m1 = H, Nyquist column kept (m2 = W/2 + 1)
+    (2, 1, 2, 16, 4, 3, 2),      # tall, k2 = 0 and the last-but-Nyquist column
+    (1, 2, 2, 4, 16, 1, 9),      # wide, every column incl. Nyquist
+]
+
+
+@pytest.mark.parametrize("shape", BACKWARD_SHAPES)
+def test_backward_input_is_the_adjoint(shape):
+    B, Cin, Cout, H, W, m1, m2 = shape
+    x = RNG.standard_normal((B, Cin, H, W))
+    g = RNG.standard_normal((B, Cout, H, W))
+    w = rand_w(Cin, Cout, m1, m2)
+    y = oracle.spectral_conv2d(x, w, m1, m2)
+    gx, _ = oracle.spectral_conv2d_backward(x, w, g, m1, m2)
+    lhs, rhs = np.sum(y * g), np.sum(x * gx)
+    assert abs(lhs - rhs) <= 1e-12 * (abs(lhs) + np.abs(y * g).sum())
+
+
+@pytest.mark.parametrize("shape", BACKWARD_SHAPES)
+def test_weight_gradient_identity(shape):
+    # y is linear in w, so <y(x, v), g> = Re sum conj(gw) * v for every v
+    B, Cin, Cout, H, W, m1, m2 = shape
+    x = RNG.standard_normal((B, Cin, H, W))
+    g = RNG.standard_normal((B, Cout, H, W))
+    w = rand_w(Cin, Cout, m1, m2)
+    v = rand_w(Cin, Cout, m1, m2)
+    _, gw = oracle.spectral_conv2d_backward(x, w, g, m1, m2)
+    lhs = np.sum(oracle.spectral_conv2d(x, v, m1, m2) * g)
+    rhs = np.real(np.sum(np.conj(gw) * v))
+    assert abs(lhs - rhs) <= 1e-12 * np.abs(np.conj(gw) * v).sum()
+
+
+def test_backward_finite_differences():
+    # central differences of L = <y, g> in one element of x, and in the real and
+    # imaginary parts of one weight of each column kind (k2 = 0, interior, Nyquist)
+    B, Cin, Cout, H, W, m1, m2 = 1, 2, 2, 8, 8, 2, 5
+    x = RNG.standard_normal((B, Cin, H, W))
+    g = RNG.standard_normal((B, Cout, H, W))
+    w = rand_w(Cin, Cout, m1, m2)
+    gx, gw = oracle.spectral_conv2d_backward(x, w, g, m1, m2)
+    L = lambda xx, ww: np.sum(oracle.spectral_conv2d(xx, ww, m1, m2) * g)  # noqa: E731
+    eps = 1e-4
+    for idx in [(0, 1, 3, 5), (0, 0, 0, 0), (0, 1, 7, 2)]:
+        dx = np.zeros_like(x)
+        dx[idx] = eps
+        fd = (L(x + dx, w) - L(x - dx, w)) / (2 * eps)
+        assert abs(fd - gx[idx]) < 1e-7 * max(1.0, abs(fd))
+    for widx in [(1, 0, 1, 0), (0, 1, 2, 3), (1, 1, 3, 4)]:
+        for unit in (1.0, 1j):
+            dw = np.zeros_like(w)
+            dw[widx] = eps * unit
+            fd = (L(x, w + dw) - L(x, w - dw)) / (2 * eps)
+            want = gw[widx].real if unit == 1.0 else gw[widx].imag
+            assert abs(fd - want) < 1e-7 * max(1.0, abs(fd))
+
+
+def test_backward_modes_weights_columns():
+    # dL/dZ is c(k2) times the truncated DFT of g: c = 1 for k2 = 0 and k2 = W/2
+    g = RNG.standard_normal((1, 1, 8, 8))
+    G = oracle.backward_modes(g, 2, 5)
+    F = np.fft.rfft2(g, norm="ortho")[:, :, kept_rows(8, 2), :5]
+    c = np.array([1.0, 2.0, 2.0, 2.0, 1.0])
+    assert np.allclose(G, F * c, rtol=1e-12, atol=1e-12)
+
+
+def test_mix_adjoint_and_weight_grad_match_numpy():
+    B, Cin, Cout, nm = 3, 4, 5, 7
+    G = RNG.standard_normal((B, Cout, nm)) + 1j * RNG.standard_normal((B, Cout, nm))
+    X = RNG.standard_normal((B, Cin, nm)) + 1j * RNG.standard_normal((B, Cin, nm))
+    w = RNG.standard_normal((Cin, Cout, nm)) + 1j * RNG.standard_normal((Cin, Cout, nm))
+    assert np.allclose(oracle.mix_adjoint(G, w), np.einsum("bom,iom->bim", G, np.conj(w)),
+                       rtol=1e-12, atol=1e-12)
+    assert np.allclose(oracle.weight_grad(X, G), np.einsum("bim,bom->iom", np.conj(X), G),
+                       rtol=1e-12, atol=1e-12)
