@@ -94,7 +94,8 @@ void set_kernel(fno_plan_s* p, int k, const char* name, size_t bytes, size_t flo
 
 const char* mix_name(const fno_plan_s* p) {
     if (p->mix_path == 2) return p->tc_split == 3 ? "mix_tc_3xtf32" : "mix_tc_tf32";
-    if (p->mix_path == 3) return "mix_wide";
+    if (p->mix_path == 3) return p->adjoint ? "mix_wide_adj" : "mix_wide";
+    if (p->mix_path == 4) return "mix_adj_fma";
     return p->mix_path == 1 ? "mix_tma" : "mix_fma";
 }
 
@@ -141,6 +142,7 @@ cudaError_t run_mix(const fno_plan_s& p, const float2* X, const float2* w, float
                     fno_launch_ctx* ctx) {
     if (p.mix_path == 2) return launch_mix_tc(p, X, w, Z, p.tc_split, s, ctx);
     if (p.mix_path == 3) return launch_mix_wide(p, X, w, Z, s, ctx);
+    if (p.mix_path == 4) return launch_mix_adjoint_fma(p, X, w, Z, s, ctx);
     return p.mix_path == 1 ? launch_mix_tma(p, X, w, Z, s, ctx) : launch_mix_modes(p, X, w, Z, s, ctx);
 }
 
@@ -152,6 +154,9 @@ fno_status_t cuda_status(cudaError_t e) {
 
 std::once_flag g_init_once;
 cudaError_t g_init_err = cudaSuccess;
+
+fno_plan_s* plan_new(int B, int Cin, int Cout, int H, int W, int m1, int m2,
+                     fno_precision_t prec, fno_plan_s* parent);
 
 }  // namespace
 
@@ -190,13 +195,36 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     });
     if (g_init_err != cudaSuccess) return FNO_ERR_CUDA;
 
+    fno_plan_s* p = plan_new(B, Cin, Cout, H, W, m1, m2, prec, nullptr);
+    if (!p) return FNO_ERR_CUDA;
+    // the backward's plan: channels swapped, contraction with w conjugated and
+    // transposed, tables and error word shared with this plan
+    p->adj = plan_new(B, Cout, Cin, H, W, m1, m2, FNO_PREC_FP32, p);
+    if (!p->adj) {
+        fno_plan_destroy(p);
+        return FNO_ERR_CUDA;
+    }
+    *out = p;
+    return FNO_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// A plan for (B, Cin, Cout, ...).  With a parent, it is that plan's adjoint:
+// the parent's tables and error word are shared and the contraction is the
+// conjugate-transpose one (fp32).  Returns nullptr on a CUDA error.
+fno_plan_s* plan_new(int B, int Cin, int Cout, int H, int W, int m1, int m2,
+                     fno_precision_t prec, fno_plan_s* parent) {
     fno_plan_s* p = new fno_plan_s();
     std::memset(p, 0, sizeof(*p));
     p->B = B; p->Cin = Cin; p->Cout = Cout; p->H = H; p->W = W; p->m1 = m1; p->m2 = m2;
+    p->adjoint = parent != nullptr;
     p->nm = 2 * m1 * m2;
     p->prec = prec;
     p->scale = (float)(1.0 / std::sqrt((double)H * (double)W));
-    if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return FNO_ERR_CUDA; }
+    if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return nullptr; }
 
     int Rf = 0, Ri = 0;
     p->path = fused_supported(W, H, m1, m2, &Rf, &Ri) ? 1 : 0;
@@ -214,6 +242,7 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     if (prec != FNO_PREC_FP32 && Cin >= 32 && Cout >= 32 &&
         mix_tc_supported(B, Cin, Cout, p->nm, p->tc_split))
         p->mix_path = 2;
+    if (p->adjoint) p->mix_path = mix_wide_supported(B, Cin, Cout, p->nm) ? 3 : 4;
 
     // workspace: X | Z | T (T only on the shape-generic path)
     size_t off = 0;
@@ -237,6 +266,13 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
                       mix_name(p));
     }
 
+    if (parent) {
+        p->shares_tables = true;
+        p->tw_h = parent->tw_h;
+        p->tw_w = parent->tw_w;
+        p->err = parent->err;
+        return p;
+    }
     std::vector<float2> th = twiddles(H), tw = twiddles(W);
     cudaError_t e = cudaMalloc(&p->tw_h, sizeof(float2) * H);
     if (e == cudaSuccess) e = cudaMalloc(&p->tw_w, sizeof(float2) * W);
@@ -246,11 +282,14 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     if (e == cudaSuccess) e = cudaMemset(p->err, 0, sizeof(unsigned));
     if (e != cudaSuccess) {
         fno_plan_destroy(p);
-        return FNO_ERR_CUDA;
+        return nullptr;
     }
-    *out = p;
-    return FNO_OK;
+    return p;
 }
+
+}  // namespace
+
+extern "C" {
 
 fno_status_t fno_plan_workspace_size(fno_plan_t p, size_t* bytes) {
     if (!p || !bytes) return FNO_ERR_INVALID_ARG;
@@ -294,11 +333,59 @@ fno_status_t fno_plan_describe(fno_plan_t p, char* buf, size_t len) {
 
 fno_status_t fno_plan_destroy(fno_plan_t p) {
     if (!p) return FNO_OK;
-    if (p->tw_h) cudaFree(p->tw_h);
-    if (p->tw_w) cudaFree(p->tw_w);
-    if (p->err) cudaFree(p->err);
+    if (p->adj) fno_plan_destroy(p->adj);
+    if (!p->shares_tables) {
+        if (p->tw_h) cudaFree(p->tw_h);
+        if (p->tw_w) cudaFree(p->tw_w);
+        if (p->err) cudaFree(p->err);
+    }
     delete p;
     return FNO_OK;
+}
+
+fno_status_t fno_plan_backward(fno_plan_t p, const float* x, const void* w, const float* gy,
+                               float* gx, void* gw, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (!p || !p->adj) return FNO_ERR_INVALID_ARG;
+    if (!gx && !gw) return FNO_ERR_INVALID_ARG;
+    fno_status_t st;
+    if ((st = check_device(p)) != FNO_OK) return st;
+    if ((st = check_ptr(gy, true)) != FNO_OK) return st;
+    if ((st = check_ptr(w, gx != nullptr)) != FNO_OK) return st;
+    if ((st = check_ptr(x, gw != nullptr)) != FNO_OK) return st;
+    if ((st = check_ptr(gx, false)) != FNO_OK) return st;
+    if ((st = check_ptr(gw, false)) != FNO_OK) return st;
+    if ((st = check_ws(p, ws, ws_bytes)) != FNO_OK) return st;
+    // outputs overlap no input, no other output and not the workspace
+    const void* ins[3] = {x, w, gy};
+    const size_t in_bytes[3] = {x_bytes(p), w_bytes(p), y_bytes(p)};
+    const void* outs[2] = {gx, gw};
+    const size_t out_bytes[2] = {x_bytes(p), w_bytes(p)};
+    for (int o = 0; o < 2; ++o) {
+        if (!outs[o]) continue;
+        for (int i = 0; i < 3; ++i)
+            if (ins[i] && overlaps(outs[o], out_bytes[o], ins[i], in_bytes[i]))
+                return FNO_ERR_INVALID_ARG;
+        if (p->ws_bytes && overlaps(outs[o], out_bytes[o], ws, p->ws_bytes))
+            return FNO_ERR_INVALID_ARG;
+    }
+    if (gx && gw && overlaps(gx, out_bytes[0], gw, out_bytes[1])) return FNO_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+        if (ins[i] && p->ws_bytes && overlaps(ws, p->ws_bytes, ins[i], in_bytes[i]))
+            return FNO_ERR_INVALID_ARG;
+
+    const fno_plan_s& q = *p->adj;  // B, Cout -> Cin, w conjugated and transposed
+    char* base = static_cast<char*>(ws);
+    float2* A = reinterpret_cast<float2*>(base + p->off_X);  // B*Cin*nm: dL/dX, then X
+    float2* G = reinterpret_cast<float2*>(base + p->off_Z);  // B*Cout*nm: forward modes of gy
+    float2* T = reinterpret_cast<float2*>(base + p->off_T);
+    cudaError_t e = run_forward(q, gy, G, T, s, nullptr);
+    if (e == cudaSuccess && gx) e = run_mix(q, G, static_cast<const float2*>(w), A, s, nullptr);
+    if (e == cudaSuccess && gx) e = run_inverse(q, A, gx, T, s, nullptr);
+    if (e == cudaSuccess && gw) e = run_forward(*p, x, A, T, s, nullptr);
+    if (e == cudaSuccess && gw)
+        e = launch_wgrad(A, G, static_cast<float2*>(gw), p->B, p->Cin, p->Cout, p->nm, p->m2,
+                         p->W, s);
+    return cuda_status(e);
 }
 
 fno_status_t fno_plan_execute(fno_plan_t p, const float* x, const void* w, float* y, void* ws,

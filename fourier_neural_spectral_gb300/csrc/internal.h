@@ -45,7 +45,12 @@ struct fno_plan_s {
     // workspace layout (byte offsets, each 256-byte aligned)
     size_t off_X, off_Z, off_T, ws_bytes;
     int path;               // 0: shape-generic kernels, 1: fused transform kernels
-    int mix_path;           // 0: mix_fma, 1: mix_tma, 2: mix_tc (tcgen05), 3: mix_wide
+    int mix_path;           // 0: mix_fma, 1: mix_tma, 2: mix_tc (tcgen05), 3: mix_wide,
+                            // 4: mix_adj_fma (adjoint plans only)
+    bool adjoint;           // contraction with w conjugated and transposed (backward's
+                            // plan: Cin, Cout are w's Cout, Cin)
+    fno_plan_s* adj;        // the backward's plan (channels swapped), owned
+    bool shares_tables;     // tw_h, tw_w and err belong to the parent plan
     int tc_split;           // mix_tc: 1 (TF32) or 3 (split TF32, hi*hi + hi*lo + lo*hi)
     int R, P;               // fused path, forward: column length per CTA and H / R
     int Ri, Pi;             // fused path, inverse: the same
@@ -86,6 +91,12 @@ cudaError_t mix_wide_init();
 bool mix_wide_supported(int B, int Cin, int Cout, int nm);
 cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                             cudaStream_t s, fno_launch_ctx* ctx);
+
+// Backward-only kernels (backward.cu).
+cudaError_t launch_wgrad(const float2* X, const float2* G, float2* gw, int B, int Cin, int Cout,
+                         int nm, int m2, int W, cudaStream_t s);
+cudaError_t launch_mix_adjoint_fma(const fno_plan_s& p, const float2* G, const float2* w,
+                                   float2* GX, cudaStream_t s, fno_launch_ctx* ctx);
 
 // tcgen05 tensor-core contraction (mix_tc.cu).
 cudaError_t mix_tc_init();

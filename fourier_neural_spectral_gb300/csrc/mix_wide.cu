@@ -72,7 +72,14 @@ size_t wide_smem(int bt) {
 // TMA once every consumer warp has released it (per-stage "empty" mbarrier),
 // so consumer warps never wait for one another.  Input channels past Cin in
 // the last stage arrive as zeros (TMA fill) and add nothing.
-template <int BT>
+//
+// ADJ (the backward's adjoint contraction, GX[b,i,m] = sum_o G[b,o,m] conj(w[i,o,m])):
+// the reduction runs over w's output channels and the CTA's 8 output channels
+// are w's input channels.  The tensor map over w is the same; only the box
+// order changes (32 modes x IC reduction channels x 8 outputs, landing as
+// [8][IC][32 modes]), and w is conjugated in the product.  Cin / Cout below are
+// the reduction and output channel counts of the launch.
+template <int BT, bool ADJ>
 __global__ void __launch_bounds__(WideTile<BT>::Threads, 4)
 mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 float2* __restrict__ Z, int B, int Cin, int Cout, int NM,
@@ -110,7 +117,10 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                     break;
                 unsigned char* st = stages + (size_t)s * T::StageBytes;
                 mbar_arrive_expect_tx(&full[s], T::StageBytes);
-                tma_load_3d(st, &tmW, 2 * m0, o0, c * IC, &full[s]);
+                if (ADJ)
+                    tma_load_3d(st, &tmW, 2 * m0, c * IC, o0, &full[s]);
+                else
+                    tma_load_3d(st, &tmW, 2 * m0, o0, c * IC, &full[s]);
                 tma_load_3d(st + T::WBytes, &tmX, 2 * m0, c * IC, b0, &full[s]);
                 issued = c + 1;
             }
@@ -134,15 +144,20 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         const int s = c % kNST;
         if (!wait_parity_bounded(&full[s], (uint32_t)((c / kNST) & 1), err)) return;
         const unsigned char* st = stages + (size_t)s * T::StageBytes;
-        // w stage [IC][kOCB][32 modes], X stage [BT][IC][32 modes]
-        const float2* Ws = reinterpret_cast<const float2*>(st) + (oh * kJO) * kModes + lane;
+        // w stage [IC][kOCB][32 modes] ([kOCB][IC][32 modes] when ADJ),
+        // X stage [BT][IC][32 modes]
+        const float2* Ws = reinterpret_cast<const float2*>(st) +
+                           (ADJ ? oh * kJO * IC : oh * kJO) * kModes + lane;
         const float2* Xs =
             reinterpret_cast<const float2*>(st + T::WBytes) + (bh * JB) * IC * kModes + lane;
 #pragma unroll
         for (int ii = 0; ii < IC; ++ii) {
             float2 wv[kJO], xv[JB];
 #pragma unroll
-            for (int j = 0; j < kJO; ++j) wv[j] = Ws[(ii * kOCB + j) * kModes];
+            for (int j = 0; j < kJO; ++j) {
+                wv[j] = Ws[(ADJ ? j * IC + ii : ii * kOCB + j) * kModes];
+                if (ADJ) wv[j].y = -wv[j].y;
+            }
 #pragma unroll
             for (int bb = 0; bb < JB; ++bb) xv[bb] = Xs[(bb * IC + ii) * kModes];
 #pragma unroll
@@ -171,16 +186,28 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 
 template <int BT>
 cudaError_t set_attr() {
-    return cudaFuncSetAttribute(mix_wide_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)WideTile<BT>::Smem);
+    cudaError_t e = cudaFuncSetAttribute(mix_wide_kernel<BT, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)WideTile<BT>::Smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mix_wide_kernel<BT, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)WideTile<BT>::Smem);
+    return e;
 }
 
+// Cin / Cout of the plan are the launch's reduction and output channel counts
+// (an adjoint plan has them swapped relative to w).
 template <int BT>
 void launch_bt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, const fno_plan_s& p,
                cudaStream_t s) {
     const dim3 grid((p.nm + kModes - 1) / kModes, (p.Cout + kOCB - 1) / kOCB, (p.B + BT - 1) / BT);
-    mix_wide_kernel<BT><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
-        mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.err);
+    if (p.adjoint)
+        mix_wide_kernel<BT, true><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
+            mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.err);
+    else
+        mix_wide_kernel<BT, false><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
+            mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.err);
 }
 
 // 3D tensor map over a complex64 array [d2][d1][NM] viewed as floats: dims
@@ -231,9 +258,12 @@ cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* 
         case 8: ic = WideTile<8>::IC; break;
         default: ic = WideTile<16>::IC; break;
     }
+    // w is [Cin_w][Cout_w][NM]: for an adjoint plan Cin_w = p.Cout (its outputs)
+    // and Cout_w = p.Cin (its reduction), boxes (32 modes, IC, 8)
     CUtensorMap mw, mx;
-    if (!encode_wide_map(&mw, w, p.nm, p.Cout, p.Cin, kOCB, ic) ||
-        !encode_wide_map(&mx, X, p.nm, p.Cin, p.B, ic, bt))
+    const bool ok_w = p.adjoint ? encode_wide_map(&mw, w, p.nm, p.Cin, p.Cout, ic, kOCB)
+                                : encode_wide_map(&mw, w, p.nm, p.Cout, p.Cin, kOCB, ic);
+    if (!ok_w || !encode_wide_map(&mx, X, p.nm, p.Cin, p.B, ic, bt))
         return cudaErrorInvalidValue;
     switch (bt) {
         case 1: launch_bt<1>(mw, mx, Z, p, s); break;

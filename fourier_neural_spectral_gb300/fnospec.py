@@ -34,7 +34,7 @@ EXPORTS = (
     "fno_status_string", "fno_plan_create", "fno_plan_workspace_size", "fno_plan_launch_count",
     "fno_plan_describe", "fno_plan_kernel_info", "fno_plan_record_events", "fno_plan_execute", "fno_plan_destroy", "fno_spectral_conv2d",
     "fno_release_cache", "fno_forward_modes", "fno_mix_modes", "fno_inverse_modes",
-    "fno_get_device_status", "fno_spectral_conv2d_noalloc",
+    "fno_get_device_status", "fno_spectral_conv2d_noalloc", "fno_plan_backward",
 )
 
 
@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH):
             "fno_inverse_modes": (st, [vp, vp, vp, vp, sz, vp]),
             "fno_get_device_status": (st, [vp, vp]),
             "fno_spectral_conv2d_noalloc": (st, [vp, vp, vp, i, i, i, i, i, i, i, vp]),
+            "fno_plan_backward": (st, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -195,6 +196,16 @@ class Plan:
                                                 _stream(stream)), "fno_inverse_modes")
         return y
 
+    def fno_plan_backward(self, x, w, gy, gx=None, gw=None, workspace=None, stream=None):
+        """dL/dx into gx and dL/dRe(w) + i dL/dIm(w) into gw (either may be None)
+        from gy = dL/dy; see include/fnospec.h."""
+        wp, wn = self._ws(workspace)
+        _check(load_library().fno_plan_backward(
+            self._h, _ptr(x), None if w is None else _weight_ptr(w), _ptr(gy), _ptr(gx),
+            None if gw is None else _weight_ptr(gw), wp, wn, _stream(stream)),
+            "fno_plan_backward")
+        return gx, gw
+
     def fno_plan_record_events(self, events):
         """Arm per-kernel timing with a list of launches + 1 torch.cuda.Event
         (created with enable_timing=True and already recorded once so that the
@@ -246,6 +257,53 @@ def spectral_conv2d(x: torch.Tensor, w: torch.Tensor, m1: int, m2: int, out=None
     if out is None:
         out = torch.empty((B, Cout, H, W), dtype=torch.float32, device=x.device)
     return fno_spectral_conv2d(x, w, out, B, Cin, Cout, H, W, m1, m2, stream)
+
+
+_autograd_plans = {}
+
+
+def _autograd_plan(B, Cin, Cout, H, W, m1, m2, device):
+    key = (B, Cin, Cout, H, W, m1, m2, device)
+    plan = _autograd_plans.get(key)
+    if plan is None:
+        with torch.cuda.device(device):
+            plan = Plan(B, Cin, Cout, H, W, m1, m2)
+        _autograd_plans[key] = plan
+    return plan
+
+
+class SpectralConv2dFunction(torch.autograd.Function):
+    """y = layer(x, w) with gradients for x (float32 [B, Cin, H, W]) and w
+    (complex64 [Cin, Cout, 2*m1, m2]) through fno_plan_execute and
+    fno_plan_backward.  Plans are cached per (shape, device); calls with the
+    same shape share the plan's workspace and run on the current stream."""
+
+    @staticmethod
+    def forward(ctx, x, w, m1, m2):
+        B, Cin, H, W = x.shape
+        Cout = w.shape[1]
+        plan = _autograd_plan(B, Cin, Cout, H, W, m1, m2, x.device.index)
+        y = torch.empty((B, Cout, H, W), dtype=torch.float32, device=x.device)
+        plan.fno_plan_execute(x, w, y)
+        ctx.save_for_backward(x, w)
+        ctx.plan = plan
+        return y
+
+    @staticmethod
+    def backward(ctx, gy):
+        x, w = ctx.saved_tensors
+        gy = gy.contiguous()
+        gx = torch.empty_like(x) if ctx.needs_input_grad[0] else None
+        gw = torch.empty_like(w) if ctx.needs_input_grad[1] else None
+        if gx is None and gw is None:
+            return None, None, None, None
+        ctx.plan.fno_plan_backward(x, w, gy, gx, gw)
+        return gx, gw, None, None
+
+
+def spectral_conv2d_autograd(x: torch.Tensor, w: torch.Tensor, m1: int, m2: int):
+    """Differentiable layer (see SpectralConv2dFunction)."""
+    return SpectralConv2dFunction.apply(x, w, m1, m2)
 
 
 def fno_release_cache():

@@ -114,6 +114,26 @@ fno_status_t fno_plan_record_events(fno_plan_t plan, cudaEvent_t* events, int co
 fno_status_t fno_plan_execute(fno_plan_t plan, const float* x, const void* w, float* y,
                               void* workspace, size_t workspace_bytes, cudaStream_t s);
 
+/* Backward of the layer for a real loss L, given gy = dL/dy (float
+ * [B][Cout][H][W]), on stream s:
+ *   gx = dL/dx, float [B][Cin][H][W]: the layer applied to gy with w conjugated
+ *        and transposed per mode (w^H[o][i] = conj(w[i][o]));
+ *   gw = dL/dRe(w) + i dL/dIm(w), complex64 [Cin][Cout][2*m1][m2]:
+ *        gw[i][o][r][k2] = c(k2) * sum_b conj(X[b][i][r][k2]) * G[b][o][r][k2],
+ *        X and G the forward modes (fno_forward_modes) of x and of gy, c = 1 for
+ *        k2 = 0 and k2 = W/2 and 2 for every other column (the Hermitian
+ *        weights of the complex-to-real step).
+ * Derived by differentiating the layer defined in the TurboFNO page, sections
+ * 2.2 and 3.1 (truncated orthonormal rfft2, per-mode product, irfft2).
+ * Either gx or gw may be NULL (that gradient is skipped, and x, respectively w,
+ * may then be NULL too); at least one must be given.  Uses the plan's workspace
+ * (fno_plan_workspace_size bytes, the same as the forward).  Outputs must not
+ * overlap x, w, gy, each other or the workspace (FNO_ERR_INVALID_ARG).  The
+ * backward computes in fp32 whatever the plan's precision. */
+fno_status_t fno_plan_backward(fno_plan_t plan, const float* x, const void* w, const float* gy,
+                               float* gx, void* gw, void* workspace, size_t workspace_bytes,
+                               cudaStream_t s);
+
 /* Release the plan's tables and error word.  Safe on NULL.  The caller must make
  * sure no work that uses the plan is still running. */
 fno_status_t fno_plan_destroy(fno_plan_t plan);
