@@ -400,6 +400,90 @@ def run_ours(args, cfg):
         dist.destroy_process_group()
 
 
+def run_ours_backward(args, cfg):
+    """Time fno_plan_backward (both gradients) on the workload; one JSON line.
+
+    Algorithmic bytes per step: x and gy read, w read (adjoint contraction),
+    gx and gw written.  Flops: the adjoint contraction and the weight gradient,
+    8*B*Cin*Cout*nm each."""
+    import torch
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__ as g
+    g.build()
+    from fourier_neural_spectral_gb300 import fnospec
+
+    peaks, peak_kind = read_peaks()
+    plan = fnospec.Plan(cfg.B, cfg.Cin, cfg.Cout, cfg.H, cfg.W, cfg.m1, cfg.m2)
+    step_bytes = 2 * cfg.x_bytes() + cfg.y_bytes() + 2 * cfg.w_bytes()
+    nsets = max(1, min(8, -(-3 * L2_BYTES // step_bytes) + 1)) if step_bytes < 3 * L2_BYTES else 1
+    x0, w0 = synth.make_inputs(cfg)
+    xs = [torch.from_numpy(x0).to(dev)]
+    for k in range(1, nsets):
+        xs.append(torch.roll(xs[0], shifts=k, dims=0).contiguous())
+    wt = torch.from_numpy(w0).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(0)
+    gys = [torch.randn((cfg.B, cfg.Cout, cfg.H, cfg.W), device=dev, generator=gen)
+           for _ in range(nsets)]  # dL/dy: seeded N(0,1)
+    gxs = [torch.empty_like(xs[0]) for _ in range(nsets)]
+    gws = [torch.empty_like(wt) for _ in range(nsets)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        j = i % nsets
+        plan.fno_plan_backward(xs[j], wt, gys[j], gxs[j], gws[j], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if plan.fno_get_device_status() != fnospec.FNO_OK:
+        raise RuntimeError("device status not clean after warm-up")
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    if plan.fno_get_device_status() != fnospec.FNO_OK:
+        raise RuntimeError("device status not clean after timed steps")
+    ms_per_step = elapsed_ms / args.steps
+    hbm = float(peaks["hbm_gbs"])
+    t_roof = step_bytes / (hbm * 1e9)
+    if rank == 0:
+        cfgd = config_dict(cfg, "fp32")
+        cfgd["pass"] = "backward (dL/dx and dL/dw)"
+        line = {
+            "metric": "FNO spectral-conv backward samples/s", "value":
+                aggregate_value(world, cfg.B, args.steps, elapsed_ms),
+            "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfgd,
+            "layer_roofline": {"bound": "hbm", "bytes_per_step": step_bytes,
+                               "t_roof_us": t_roof * 1e6, "t_step_us": ms_per_step * 1e3,
+                               "frac": t_roof / (ms_per_step * 1e-3), "peak_gbs": hbm,
+                               "peak_kind": peak_kind},
+            "plan": plan.description, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -409,12 +493,16 @@ def main():
     ap.add_argument("--precision", default="fp32", choices=["fp32", "tf32", "3xtf32"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
+                    help="forward (the headline) or the layer's backward (fp32)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     cfg = synth.CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif args.pass_ == "backward":
+        run_ours_backward(args, cfg)
     else:
         run_ours(args, cfg)
 

@@ -383,8 +383,9 @@ fno_status_t fno_plan_backward(fno_plan_t p, const float* x, const void* w, cons
     if (e == cudaSuccess && gx) e = run_inverse(q, A, gx, T, s, nullptr);
     if (e == cudaSuccess && gw) e = run_forward(*p, x, A, T, s, nullptr);
     if (e == cudaSuccess && gw)
-        e = launch_wgrad(A, G, static_cast<float2*>(gw), p->B, p->Cin, p->Cout, p->nm, p->m2,
-                         p->W, s);
+        e = p->nm >= 32 ? launch_wgrad_wide(*p, A, G, static_cast<float2*>(gw), s)
+                        : launch_wgrad(A, G, static_cast<float2*>(gw), p->B, p->Cin, p->Cout,
+                                       p->nm, p->m2, p->W, s);
     return cuda_status(e);
 }
 

@@ -91,6 +91,8 @@ cudaError_t mix_wide_init();
 bool mix_wide_supported(int B, int Cin, int Cout, int nm);
 cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                             cudaStream_t s, fno_launch_ctx* ctx);
+cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2* G, float2* gw,
+                              cudaStream_t s);
 
 // Backward-only kernels (backward.cu).
 cudaError_t launch_wgrad(const float2* X, const float2* G, float2* gw, int B, int Cin, int Cout,

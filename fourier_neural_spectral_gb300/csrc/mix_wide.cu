@@ -73,16 +73,25 @@ size_t wide_smem(int bt) {
 // so consumer warps never wait for one another.  Input channels past Cin in
 // the last stage arrive as zeros (TMA fill) and add nothing.
 //
-// ADJ (the backward's adjoint contraction, GX[b,i,m] = sum_o G[b,o,m] conj(w[i,o,m])):
-// the reduction runs over w's output channels and the CTA's 8 output channels
-// are w's input channels.  The tensor map over w is the same; only the box
-// order changes (32 modes x IC reduction channels x 8 outputs, landing as
-// [8][IC][32 modes]), and w is conjugated in the product.  Cin / Cout below are
-// the reduction and output channel counts of the launch.
-template <int BT, bool ADJ>
+// The same pipeline serves three products (MODE); rows / red / Cout below are
+// the launch's row count, reduction length and output channel count:
+//   kMix   Z[b,o,m] = sum_i X[b,i,m] w[i,o,m]          rows b, reduction i;
+//   kAdj   GX[b,i,m] = sum_o G[b,o,m] conj(w[i,o,m])   (the backward's adjoint
+//          contraction) rows b, reduction over w's output channels, outputs
+//          w's input channels: same tensor map over w, box order (32 modes x
+//          IC reductions x 8 outputs) landing as [8][IC][32 modes];
+//   kWgrad gw[i,o,m] = c(k2) sum_b conj(X[b,i,m]) G[b,o,m]  (the weight
+//          gradient) rows i, reduction b: the "w" operand is G [B][Cout][NM]
+//          (box 32 modes x 8 outputs x IC batch rows, as kMix) and the "X"
+//          operand is X [B][Cin][NM] with box 32 modes x BT rows x IC batch
+//          rows, landing as [IC][BT][32 modes]; c = 1 at k2 = 0 and k2 = W/2,
+//          else 2.
+enum { kMix = 0, kAdj = 1, kWgrad = 2 };
+
+template <int BT, int MODE>
 __global__ void __launch_bounds__(WideTile<BT>::Threads, 4)
 mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                float2* __restrict__ Z, int B, int Cin, int Cout, int NM,
+                float2* __restrict__ Z, int rows, int red, int Cout, int NM, int m2, int W,
                 unsigned* __restrict__ err) {
     using T = WideTile<BT>;
     constexpr int JB = T::JB, IC = T::IC;
@@ -92,7 +101,7 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     unsigned char* stages = smem + 128;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m0 = blockIdx.x * kModes, o0 = blockIdx.y * kOCB, b0 = blockIdx.z * BT;
-    const int nch = (Cin + IC - 1) / IC;
+    const int nch = (red + IC - 1) / IC;
 
     if (tid == 0) {
         for (int s = 0; s < kNST; ++s) {
@@ -117,11 +126,14 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                     break;
                 unsigned char* st = stages + (size_t)s * T::StageBytes;
                 mbar_arrive_expect_tx(&full[s], T::StageBytes);
-                if (ADJ)
+                if (MODE == kAdj)
                     tma_load_3d(st, &tmW, 2 * m0, c * IC, o0, &full[s]);
                 else
                     tma_load_3d(st, &tmW, 2 * m0, o0, c * IC, &full[s]);
-                tma_load_3d(st + T::WBytes, &tmX, 2 * m0, c * IC, b0, &full[s]);
+                if (MODE == kWgrad)
+                    tma_load_3d(st + T::WBytes, &tmX, 2 * m0, b0, c * IC, &full[s]);
+                else
+                    tma_load_3d(st + T::WBytes, &tmX, 2 * m0, c * IC, b0, &full[s]);
                 issued = c + 1;
             }
             // no copy may be in flight when the CTA leaves: the last kNST issued
@@ -144,22 +156,25 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         const int s = c % kNST;
         if (!wait_parity_bounded(&full[s], (uint32_t)((c / kNST) & 1), err)) return;
         const unsigned char* st = stages + (size_t)s * T::StageBytes;
-        // w stage [IC][kOCB][32 modes] ([kOCB][IC][32 modes] when ADJ),
-        // X stage [BT][IC][32 modes]
+        // w stage [IC][kOCB][32 modes] ([kOCB][IC][32 modes] for kAdj),
+        // X stage [BT][IC][32 modes] ([IC][BT][32 modes] for kWgrad)
         const float2* Ws = reinterpret_cast<const float2*>(st) +
-                           (ADJ ? oh * kJO * IC : oh * kJO) * kModes + lane;
-        const float2* Xs =
-            reinterpret_cast<const float2*>(st + T::WBytes) + (bh * JB) * IC * kModes + lane;
+                           (MODE == kAdj ? oh * kJO * IC : oh * kJO) * kModes + lane;
+        const float2* Xs = reinterpret_cast<const float2*>(st + T::WBytes) +
+                           (MODE == kWgrad ? bh * JB : bh * JB * IC) * kModes + lane;
 #pragma unroll
         for (int ii = 0; ii < IC; ++ii) {
             float2 wv[kJO], xv[JB];
 #pragma unroll
             for (int j = 0; j < kJO; ++j) {
-                wv[j] = Ws[(ADJ ? j * IC + ii : ii * kOCB + j) * kModes];
-                if (ADJ) wv[j].y = -wv[j].y;
+                wv[j] = Ws[(MODE == kAdj ? j * IC + ii : ii * kOCB + j) * kModes];
+                if (MODE == kAdj) wv[j].y = -wv[j].y;
             }
 #pragma unroll
-            for (int bb = 0; bb < JB; ++bb) xv[bb] = Xs[(bb * IC + ii) * kModes];
+            for (int bb = 0; bb < JB; ++bb) {
+                xv[bb] = Xs[(MODE == kWgrad ? ii * BT + bb : bb * IC + ii) * kModes];
+                if (MODE == kWgrad) xv[bb].y = -xv[bb].y;
+            }
 #pragma unroll
             for (int j = 0; j < kJO; ++j)
 #pragma unroll
@@ -171,28 +186,37 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 
     const int m = m0 + lane;
     if (m >= NM) return;
+    float c = 1.f;
+    if (MODE == kWgrad) {
+        const int k2 = m % m2;
+        c = (k2 == 0 || 2 * k2 == W) ? 1.f : 2.f;
+    }
 #pragma unroll
     for (int j = 0; j < kJO; ++j) {
         const int o = o0 + oh * kJO + j;
         if (o >= Cout) break;
 #pragma unroll
         for (int bb = 0; bb < JB; ++bb) {
-            const int b = b0 + bh * JB + bb;
-            if (b >= B) break;
-            Z[((size_t)b * Cout + o) * NM + m] = acc[j][bb];
+            const int r = b0 + bh * JB + bb;
+            if (r >= rows) break;
+            Z[((size_t)r * Cout + o) * NM + m] = MODE == kWgrad ? cscale(acc[j][bb], c) : acc[j][bb];
         }
     }
 }
 
 template <int BT>
 cudaError_t set_attr() {
-    cudaError_t e = cudaFuncSetAttribute(mix_wide_kernel<BT, false>,
+    cudaError_t e = cudaFuncSetAttribute(mix_wide_kernel<BT, kMix>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)WideTile<BT>::Smem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mix_wide_kernel<BT, true>,
+        e = cudaFuncSetAttribute(mix_wide_kernel<BT, kAdj>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)WideTile<BT>::Smem);
+    if (e == cudaSuccess && BT == 16)
+        e = cudaFuncSetAttribute(mix_wide_kernel<16, kWgrad>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)WideTile<16>::Smem);
     return e;
 }
 
@@ -203,11 +227,11 @@ void launch_bt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, const fn
                cudaStream_t s) {
     const dim3 grid((p.nm + kModes - 1) / kModes, (p.Cout + kOCB - 1) / kOCB, (p.B + BT - 1) / BT);
     if (p.adjoint)
-        mix_wide_kernel<BT, true><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
-            mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.err);
+        mix_wide_kernel<BT, kAdj><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
+            mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, p.err);
     else
-        mix_wide_kernel<BT, false><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
-            mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.err);
+        mix_wide_kernel<BT, kMix><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
+            mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, p.err);
 }
 
 // 3D tensor map over a complex64 array [d2][d1][NM] viewed as floats: dims
@@ -275,4 +299,19 @@ cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* 
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
+}
+
+// Weight gradient gw[i][o][m] = c(k2) * sum_b conj(X[b][i][m]) * G[b][o][m] for
+// the plan p (X [B][Cin][nm], G [B][Cout][nm], gw [Cin][Cout][nm]).
+cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2* G, float2* gw,
+                              cudaStream_t s) {
+    using T = WideTile<16>;
+    CUtensorMap mg, mx;
+    if (!encode_wide_map(&mg, G, p.nm, p.Cout, p.B, kOCB, T::IC) ||
+        !encode_wide_map(&mx, X, p.nm, p.Cin, p.B, 16, T::IC))
+        return cudaErrorInvalidValue;
+    const dim3 grid((p.nm + kModes - 1) / kModes, (p.Cout + kOCB - 1) / kOCB, (p.Cin + 15) / 16);
+    mix_wide_kernel<16, kWgrad><<<grid, T::Threads, T::Smem, s>>>(mg, mx, gw, p.Cin, p.B, p.Cout,
+                                                                 p.nm, p.m2, p.W, p.err);
+    return cudaGetLastError();
 }
