@@ -100,7 +100,11 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     uint64_t* empty = full + kNST;
     unsigned char* stages = smem + 128;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int m0 = blockIdx.x * kModes, o0 = blockIdx.y * kOCB, b0 = blockIdx.z * BT;
+    // blockIdx.x enumerates (mode block, output block) with the output blocks
+    // of one mode block consecutive, so CTAs that share an X tile run together
+    const int nob = (Cout + kOCB - 1) / kOCB;
+    const int m0 = (blockIdx.x / nob) * kModes, o0 = (blockIdx.x % nob) * kOCB;
+    const int b0 = blockIdx.z * BT;
     const int nch = (red + IC - 1) / IC;
 
     if (tid == 0) {
@@ -225,7 +229,8 @@ cudaError_t set_attr() {
 template <int BT>
 void launch_bt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, const fno_plan_s& p,
                cudaStream_t s) {
-    const dim3 grid((p.nm + kModes - 1) / kModes, (p.Cout + kOCB - 1) / kOCB, (p.B + BT - 1) / BT);
+    const dim3 grid(((p.nm + kModes - 1) / kModes) * ((p.Cout + kOCB - 1) / kOCB), 1,
+                    (p.B + BT - 1) / BT);
     if (p.adjoint)
         mix_wide_kernel<BT, kAdj><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
             mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, p.err);
@@ -310,7 +315,8 @@ cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2
     if (!encode_wide_map(&mg, G, p.nm, p.Cout, p.B, kOCB, T::IC) ||
         !encode_wide_map(&mx, X, p.nm, p.Cin, p.B, 16, T::IC))
         return cudaErrorInvalidValue;
-    const dim3 grid((p.nm + kModes - 1) / kModes, (p.Cout + kOCB - 1) / kOCB, (p.Cin + 15) / 16);
+    const dim3 grid(((p.nm + kModes - 1) / kModes) * ((p.Cout + kOCB - 1) / kOCB), 1,
+                    (p.Cin + 15) / 16);
     mix_wide_kernel<16, kWgrad><<<grid, T::Threads, T::Smem, s>>>(mg, mx, gw, p.Cin, p.B, p.Cout,
                                                                  p.nm, p.m2, p.W, p.err);
     return cudaGetLastError();
