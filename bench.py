@@ -268,10 +268,14 @@ def run_ours(args, cfg):
     if plan.fno_get_device_status() != fnospec.FNO_OK:
         raise RuntimeError("device status not clean after warm-up")
 
-    # per-kernel events armed for every timed step: events[k] .. events[k+1]
+    # The timed steps run back to back with no event between their kernels
+    # (an event recorded between two kernels keeps the second from starting in
+    # the first one's tail); the per-kernel breakdown and the latency
+    # percentiles come from separate steps with per-kernel events armed.
     nk = plan.launches
+    nbreak = max(3, min(args.steps, 20))
     evsets = []
-    for _ in range(args.steps):
+    for _ in range(nbreak):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
         for e in evs:
             e.record(stream)  # materialise the CUDA events
@@ -287,9 +291,7 @@ def run_ours(args, cfg):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        plan.fno_plan_record_events(evsets[i])
         step(args.warmup + i)
-    plan.fno_plan_record_events(None)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -299,6 +301,13 @@ def run_ours(args, cfg):
     status = plan.fno_get_device_status()
     if status != fnospec.FNO_OK:
         raise RuntimeError(f"device status {status} after timed steps")
+    for i in range(nbreak):
+        plan.fno_plan_record_events(evsets[i])
+        step(args.warmup + args.steps + i)
+    plan.fno_plan_record_events(None)
+    torch.cuda.synchronize(dev)
+    if plan.fno_get_device_status() != fnospec.FNO_OK:
+        raise RuntimeError("device status not clean after the breakdown steps")
 
     per_step = [evs[0].elapsed_time(evs[-1]) for evs in evsets]
     per_kernel = [[evs[k].elapsed_time(evs[k + 1]) for evs in evsets] for k in range(nk)]
@@ -384,7 +393,7 @@ def run_ours(args, cfg):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": dtype, "data": "synthetic (seeded SplitMix64 inputs, random weights)",
             "config": cfgd, "roofline": roofline, "layer_roofline": layer,
-            "kernels": kernels, "plan": plan.description,
+            "kernels": kernels, "kernel_breakdown_steps": nbreak, "plan": plan.description,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": cfg.x_bytes(),
                     "d2h_bytes_per_step": cfg.y_bytes(),

@@ -24,6 +24,23 @@ __device__ __forceinline__ void cmac(float2& acc, float2 a, float2 b) {
 
 __device__ __forceinline__ int ilog2(int v) { return 31 - __clz(v); }
 
+// Programmatic dependent launch (PTX griddepcontrol, sm_90+).  Kernels of the
+// layer's main path are launched with programmatic stream serialisation
+// (launch_pdl in internal.h) and begin with
+//   griddep_wait();              // every earlier grid of the stream has completed
+//                                // and its writes are visible
+//   griddep_launch_dependents(); // the next grid may be scheduled
+// so the next kernel's CTAs can take SMs left idle by this kernel's last
+// wave.  Because each kernel triggers only after its own wait, when kernel k+1
+// starts, kernel k-1 and everything before it have completed: a kernel may read
+// inputs that kernel k does not produce before its own griddep_wait().
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Radix-2 Stockham autosort FFT of length L (power of two >= 2) on S sequences
 // stored back to back in shared memory (sequence s at a[s*L .. s*L + L)).
 // Stage p (p = 1, 2, 4, ..., L/2) reads a, writes b:

@@ -121,34 +121,52 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         if (lane == 0) {
             prefetch_tensormap(&tmW);
             prefetch_tensormap(&tmX);
-            int issued = 0;
-            for (int c = 0; c < nch; ++c) {
+            const auto load_w = [&](int c) {
+                unsigned char* st = stages + (size_t)(c % kNST) * T::StageBytes;
+                mbar_arrive_expect_tx(&full[c % kNST], T::StageBytes);
+                if (MODE == kAdj)
+                    tma_load_3d(st, &tmW, 2 * m0, c * IC, o0, &full[c % kNST]);
+                else
+                    tma_load_3d(st, &tmW, 2 * m0, o0, c * IC, &full[c % kNST]);
+            };
+            const auto load_x = [&](int c) {
+                unsigned char* st = stages + (size_t)(c % kNST) * T::StageBytes;
+                if (MODE == kWgrad)
+                    tma_load_3d(st + T::WBytes, &tmX, 2 * m0, b0, c * IC, &full[c % kNST]);
+                else
+                    tma_load_3d(st + T::WBytes, &tmX, 2 * m0, c * IC, b0, &full[c % kNST]);
+            };
+            // the "w" operand is never written by the kernel just before this one
+            // (w is an input; G comes from an earlier kernel), so the first
+            // stages' w boxes may be fetched before griddep_wait()
+            const int pre = nch < kNST ? nch : kNST;
+            for (int c = 0; c < pre; ++c) load_w(c);
+            griddep_wait();
+            griddep_launch_dependents();
+            for (int c = 0; c < pre; ++c) load_x(c);
+            int issued = pre;
+            for (int c = pre; c < nch; ++c) {
                 const int s = c % kNST;
                 // stage s last held chunk c - kNST: wait until every consumer let it go
-                if (c >= kNST &&
-                    !wait_parity_bounded(&empty[s], (uint32_t)((c / kNST - 1) & 1), err))
-                    break;
-                unsigned char* st = stages + (size_t)s * T::StageBytes;
-                mbar_arrive_expect_tx(&full[s], T::StageBytes);
-                if (MODE == kAdj)
-                    tma_load_3d(st, &tmW, 2 * m0, c * IC, o0, &full[s]);
-                else
-                    tma_load_3d(st, &tmW, 2 * m0, o0, c * IC, &full[s]);
-                if (MODE == kWgrad)
-                    tma_load_3d(st + T::WBytes, &tmX, 2 * m0, b0, c * IC, &full[s]);
-                else
-                    tma_load_3d(st + T::WBytes, &tmX, 2 * m0, c * IC, b0, &full[s]);
+                if (!wait_parity_bounded(&empty[s], (uint32_t)((c / kNST - 1) & 1), err)) break;
+                load_w(c);
+                load_x(c);
                 issued = c + 1;
             }
             // no copy may be in flight when the CTA leaves: the last kNST issued
             // chunks are the only ones not known to have landed (bounded waits)
             for (int c = issued > kNST ? issued - kNST : 0; c < issued; ++c)
                 wait_parity_bounded(&full[c % kNST], (uint32_t)((c / kNST) & 1), nullptr);
+        } else {
+            griddep_wait();
+            griddep_launch_dependents();
         }
         return;
     }
 
     // ---- consumers ------------------------------------------------------
+    griddep_wait();  // Z may still be read by an earlier kernel until then
+    griddep_launch_dependents();
     const int oh = warp & 1, bh = warp >> 1;
     float2 acc[kJO][JB];
 #pragma unroll
@@ -227,16 +245,16 @@ cudaError_t set_attr() {
 // Cin / Cout of the plan are the launch's reduction and output channel counts
 // (an adjoint plan has them swapped relative to w).
 template <int BT>
-void launch_bt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, const fno_plan_s& p,
-               cudaStream_t s) {
+cudaError_t launch_bt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, const fno_plan_s& p,
+                      cudaStream_t s) {
     const dim3 grid(((p.nm + kModes - 1) / kModes) * ((p.Cout + kOCB - 1) / kOCB), 1,
                     (p.B + BT - 1) / BT);
     if (p.adjoint)
-        mix_wide_kernel<BT, kAdj><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
-            mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, p.err);
-    else
-        mix_wide_kernel<BT, kMix><<<grid, WideTile<BT>::Threads, WideTile<BT>::Smem, s>>>(
-            mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, p.err);
+        return launch_pdl(mix_wide_kernel<BT, kAdj>, grid, WideTile<BT>::Threads,
+                          WideTile<BT>::Smem, s, mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W,
+                          p.err);
+    return launch_pdl(mix_wide_kernel<BT, kMix>, grid, WideTile<BT>::Threads, WideTile<BT>::Smem,
+                      s, mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, p.err);
 }
 
 // 3D tensor map over a complex64 array [d2][d1][NM] viewed as floats: dims
@@ -294,14 +312,14 @@ cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* 
                                 : encode_wide_map(&mw, w, p.nm, p.Cout, p.Cin, kOCB, ic);
     if (!ok_w || !encode_wide_map(&mx, X, p.nm, p.Cin, p.B, ic, bt))
         return cudaErrorInvalidValue;
+    cudaError_t e;
     switch (bt) {
-        case 1: launch_bt<1>(mw, mx, Z, p, s); break;
-        case 2: launch_bt<2>(mw, mx, Z, p, s); break;
-        case 4: launch_bt<4>(mw, mx, Z, p, s); break;
-        case 8: launch_bt<8>(mw, mx, Z, p, s); break;
-        default: launch_bt<16>(mw, mx, Z, p, s); break;
+        case 1: e = launch_bt<1>(mw, mx, Z, p, s); break;
+        case 2: e = launch_bt<2>(mw, mx, Z, p, s); break;
+        case 4: e = launch_bt<4>(mw, mx, Z, p, s); break;
+        case 8: e = launch_bt<8>(mw, mx, Z, p, s); break;
+        default: e = launch_bt<16>(mw, mx, Z, p, s); break;
     }
-    cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
@@ -317,7 +335,6 @@ cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2
         return cudaErrorInvalidValue;
     const dim3 grid(((p.nm + kModes - 1) / kModes) * ((p.Cout + kOCB - 1) / kOCB), 1,
                     (p.Cin + 15) / 16);
-    mix_wide_kernel<16, kWgrad><<<grid, T::Threads, T::Smem, s>>>(mg, mx, gw, p.Cin, p.B, p.Cout,
-                                                                 p.nm, p.m2, p.W, p.err);
-    return cudaGetLastError();
+    return launch_pdl(mix_wide_kernel<16, kWgrad>, grid, T::Threads, T::Smem, s, mg, mx, gw,
+                      p.Cin, p.B, p.Cout, p.nm, p.m2, p.W, p.err);
 }

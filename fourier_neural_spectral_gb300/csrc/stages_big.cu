@@ -136,6 +136,8 @@ fwd_big_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m
     constexpr int npairs = R / 2;
     float* stg = stage + g * 2 * W;
     uint64_t* bar = bars + g;
+    griddep_wait();
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < B::Groups; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
@@ -252,6 +254,8 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
     const int plane = blockIdx.x / P;
     const int p = blockIdx.x - plane * P;
     const float2* Zp = Z + (size_t)plane * 2 * m1 * m2;
+    griddep_wait();
+    griddep_launch_dependents();
 
     // ZS (big_z_staged): the plane's Z comes into shared memory with one bulk copy
     uint64_t* zbar = reinterpret_cast<uint64_t*>(V + big_y_floats2(R, m2));
@@ -365,19 +369,17 @@ cudaError_t launch(const fno_plan_s& p, const float* x, float2* X, const float2*
     if (FWD) {
         const size_t smem = big_smem_bytes<W, R, true>(p.m2);
         const unsigned grid = (unsigned)((size_t)p.B * p.Cin * p.P);
-        fwd_big_kernel<W, R><<<grid, kBT, smem, s>>>(x, X, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
-                                                     p.tw_h, p.err);
+        return launch_pdl(fwd_big_kernel<W, R>, grid, kBT, smem, s, x, X, p.H, p.m1, p.m2, p.P,
+                          p.scale, p.tw_w, p.tw_h, p.err);
     } else {
         const size_t smem = big_smem_bytes<W, R, false>(p.m2);
         const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.Pi);
         if (big_z_staged<W, R>(p.m1, p.m2))
-            inv_big_kernel<W, R, true><<<grid, kBT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.Pi, p.scale,
-                                                               p.tw_w, p.tw_h, p.err);
-        else
-            inv_big_kernel<W, R, false><<<grid, kBT, smem, s>>>(Z, y, p.H, p.m1, p.m2, p.Pi,
-                                                                p.scale, p.tw_w, p.tw_h, p.err);
+            return launch_pdl(inv_big_kernel<W, R, true>, grid, kBT, smem, s, Z, y, p.H, p.m1,
+                              p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
+        return launch_pdl(inv_big_kernel<W, R, false>, grid, kBT, smem, s, Z, y, p.H, p.m1, p.m2,
+                          p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
     }
-    return cudaGetLastError();
 }
 
 template <bool FWD, int W>

@@ -325,6 +325,8 @@ fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int
     const int plane = blockIdx.x / P;
     const int p = blockIdx.x - plane * P;
     const float* xp = x + (size_t)plane * H * W;
+    griddep_wait();
+    griddep_launch_dependents();
 
     // ---- rows -----------------------------------------------------------
     {
@@ -385,6 +387,8 @@ inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int
     const int p = blockIdx.x - plane * P;
     const int R2 = 2 * m1;
     const float2* Zp = Z + (size_t)plane * R2 * m2;
+    griddep_wait();
+    griddep_launch_dependents();
 
     // ---- columns: retained rows of Z -> V[q][col], q in [0, R) ----------
     // ZS (fused_z_staged): the plane's Z comes into shared memory first
@@ -435,6 +439,8 @@ template <int W, int R>
 constexpr bool has_static() { return W == R && (W == 64 || W == 128 || W == 256); }
 
 __global__ void zero_kernel(float4* __restrict__ p, size_t n4) {
+    griddep_wait();
+    griddep_launch_dependents();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
          i += (size_t)gridDim.x * blockDim.x)
         p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -481,14 +487,12 @@ cudaError_t launch_fwd(const fno_plan_s& p, const float* x, float2* X, cudaStrea
     const unsigned grid = (unsigned)((size_t)p.B * p.Cin * p.P);
     if constexpr (has_static<W, R>()) {
         if (p.m1 == W / 4 && p.m2 == W / 4) {
-            fwd_fused_kernel<W, R, W / 4, W / 4><<<grid, kFT, smem, s>>>(
-                x, X, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w, p.tw_h);
-            return cudaGetLastError();
+            return launch_pdl(fwd_fused_kernel<W, R, W / 4, W / 4>, grid, kFT, smem, s, x, X, p.H,
+                              p.m1, p.m2, p.P, p.scale, p.tw_w, p.tw_h);
         }
     }
-    fwd_fused_kernel<W, R><<<grid, kFT, smem, s>>>(x, X, p.H, p.m1, p.m2, p.P, p.scale, p.tw_w,
-                                                   p.tw_h);
-    return cudaGetLastError();
+    return launch_pdl(fwd_fused_kernel<W, R>, grid, kFT, smem, s, x, X, p.H, p.m1, p.m2, p.P,
+                      p.scale, p.tw_w, p.tw_h);
 }
 
 template <int W, int R, int M1S, int M2S>
@@ -496,12 +500,10 @@ cudaError_t launch_inv_zs(const fno_plan_s& p, const float2* Z, float* y, cudaSt
     const size_t smem = fused_smem_bytes<W, R>(p.m2);
     const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.Pi);
     if (zs_compiled<W, R, M2S>() && fused_z_staged<W, R>(p.m1, p.m2))
-        inv_fused_kernel<W, R, M1S, M2S, zs_compiled<W, R, M2S>()><<<grid, kFT, smem, s>>>(
-            Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
-    else
-        inv_fused_kernel<W, R, M1S, M2S, false><<<grid, kFT, smem, s>>>(
-            Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
-    return cudaGetLastError();
+        return launch_pdl(inv_fused_kernel<W, R, M1S, M2S, zs_compiled<W, R, M2S>()>, grid, kFT,
+                          smem, s, Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
+    return launch_pdl(inv_fused_kernel<W, R, M1S, M2S, false>, grid, kFT, smem, s, Z, y, p.H,
+                      p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
 }
 
 template <int W, int R>
@@ -599,9 +601,8 @@ cudaError_t launch_forward_fused(const fno_plan_s& p, const float* x, float2* X,
     cudaError_t e = cudaSuccess;
     if (p.P > 1) {
         const size_t n4 = (size_t)p.B * p.Cin * p.nm / 2;  // complex pairs -> float4
-        zero_kernel<<<std::min<size_t>((n4 + 255) / 256, 4096), 256, 0, s>>>(
-            reinterpret_cast<float4*>(X), n4);
-        e = cudaGetLastError();
+        e = launch_pdl(zero_kernel, dim3((unsigned)std::min<size_t>((n4 + 255) / 256, 4096)),
+                       dim3(256), 0, s, reinterpret_cast<float4*>(X), n4);
         if (e == cudaSuccess && ctx) e = ctx->mark(s);
         if (e != cudaSuccess) return e;
     }
