@@ -138,10 +138,11 @@ cudaError_t run_inverse(const fno_plan_s& p, const float2* Z, float* y, float2* 
     return p.path == 1 ? launch_inverse_fused(p, Z, y, s, ctx) : launch_inverse_modes(p, Z, y, T, s, ctx);
 }
 
+// after_own_forward: the previous kernel on s is this library's forward stage.
 cudaError_t run_mix(const fno_plan_s& p, const float2* X, const float2* w, float2* Z, cudaStream_t s,
-                    fno_launch_ctx* ctx) {
+                    fno_launch_ctx* ctx, bool after_own_forward) {
     if (p.mix_path == 2) return launch_mix_tc(p, X, w, Z, p.tc_split, s, ctx);
-    if (p.mix_path == 3) return launch_mix_wide(p, X, w, Z, s, ctx);
+    if (p.mix_path == 3) return launch_mix_wide(p, X, w, Z, after_own_forward, s, ctx);
     if (p.mix_path == 4) return launch_mix_adjoint_fma(p, X, w, Z, s, ctx);
     return p.mix_path == 1 ? launch_mix_tma(p, X, w, Z, s, ctx) : launch_mix_modes(p, X, w, Z, s, ctx);
 }
@@ -379,7 +380,8 @@ fno_status_t fno_plan_backward(fno_plan_t p, const float* x, const void* w, cons
     float2* G = reinterpret_cast<float2*>(base + p->off_Z);  // B*Cout*nm: forward modes of gy
     float2* T = reinterpret_cast<float2*>(base + p->off_T);
     cudaError_t e = run_forward(q, gy, G, T, s, nullptr);
-    if (e == cudaSuccess && gx) e = run_mix(q, G, static_cast<const float2*>(w), A, s, nullptr);
+    if (e == cudaSuccess && gx)
+        e = run_mix(q, G, static_cast<const float2*>(w), A, s, nullptr, true);
     if (e == cudaSuccess && gx) e = run_inverse(q, A, gx, T, s, nullptr);
     if (e == cudaSuccess && gw) e = run_forward(*p, x, A, T, s, nullptr);
     if (e == cudaSuccess && gw)
@@ -413,7 +415,7 @@ fno_status_t fno_plan_execute(fno_plan_t p, const float* x, const void* w, float
     ctx.count = p->nevents;
     cudaError_t e = ctx.mark(s);
     if (e == cudaSuccess) e = run_forward(*p, x, X, T, s, &ctx);
-    if (e == cudaSuccess) e = run_mix(*p, X, static_cast<const float2*>(w), Z, s, &ctx);
+    if (e == cudaSuccess) e = run_mix(*p, X, static_cast<const float2*>(w), Z, s, &ctx, true);
     if (e == cudaSuccess) e = run_inverse(*p, Z, y, T, s, &ctx);
     return cuda_status(e);
 }
@@ -443,7 +445,7 @@ fno_status_t fno_mix_modes(fno_plan_t p, const void* X, const void* w, void* Z, 
     if (overlaps(Z, Z_bytes(p), X, X_bytes(p)) || overlaps(Z, Z_bytes(p), w, w_bytes(p)))
         return FNO_ERR_INVALID_ARG;
     return cuda_status(run_mix(*p, static_cast<const float2*>(X), static_cast<const float2*>(w),
-                               static_cast<float2*>(Z), s, nullptr));
+                               static_cast<float2*>(Z), s, nullptr, false));
 }
 
 fno_status_t fno_inverse_modes(fno_plan_t p, const void* Z, float* y, void* ws, size_t ws_bytes,

@@ -108,8 +108,10 @@ cudaError_t launch_mix_tma(const fno_plan_s& p, const float2* X, const float2* w
 // fp32 contraction over blocks of 32 consecutive modes (mix_wide.cu).
 cudaError_t mix_wide_init();
 bool mix_wide_supported(int B, int Cin, int Cout, int nm);
+// after_own_forward: the kernel just before this one is the library's forward
+// stage (w may then be fetched before the programmatic-launch wait).
 cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
-                            cudaStream_t s, fno_launch_ctx* ctx);
+                            bool after_own_forward, cudaStream_t s, fno_launch_ctx* ctx);
 cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2* G, float2* gw,
                               cudaStream_t s);
 

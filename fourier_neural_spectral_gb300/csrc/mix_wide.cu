@@ -92,7 +92,7 @@ template <int BT, int MODE>
 __global__ void __launch_bounds__(WideTile<BT>::Threads, 4)
 mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 float2* __restrict__ Z, int rows, int red, int Cout, int NM, int m2, int W,
-                unsigned* __restrict__ err) {
+                int early_w, unsigned* __restrict__ err) {
     using T = WideTile<BT>;
     constexpr int JB = T::JB, IC = T::IC;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -136,14 +136,20 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
                 else
                     tma_load_3d(st + T::WBytes, &tmX, 2 * m0, c * IC, b0, &full[c % kNST]);
             };
-            // the "w" operand is never written by the kernel just before this one
-            // (w is an input; G comes from an earlier kernel), so the first
-            // stages' w boxes may be fetched before griddep_wait()
+            // early_w: the kernel just before this one is the library's own
+            // forward stage, which never writes the "w" operand (w is an input, G
+            // comes from an earlier kernel), so the first stages' w boxes may be
+            // fetched before griddep_wait().  Callers of the standalone stage
+            // entry point get no such guarantee and pass early_w = 0.
             const int pre = nch < kNST ? nch : kNST;
-            for (int c = 0; c < pre; ++c) load_w(c);
+            if (early_w)
+                for (int c = 0; c < pre; ++c) load_w(c);
             griddep_wait();
             griddep_launch_dependents();
-            for (int c = 0; c < pre; ++c) load_x(c);
+            for (int c = 0; c < pre; ++c) {
+                if (!early_w) load_w(c);
+                load_x(c);
+            }
             int issued = pre;
             for (int c = pre; c < nch; ++c) {
                 const int s = c % kNST;
@@ -246,15 +252,15 @@ cudaError_t set_attr() {
 // (an adjoint plan has them swapped relative to w).
 template <int BT>
 cudaError_t launch_bt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, const fno_plan_s& p,
-                      cudaStream_t s) {
+                      int early_w, cudaStream_t s) {
     const dim3 grid(((p.nm + kModes - 1) / kModes) * ((p.Cout + kOCB - 1) / kOCB), 1,
                     (p.B + BT - 1) / BT);
     if (p.adjoint)
         return launch_pdl(mix_wide_kernel<BT, kAdj>, grid, WideTile<BT>::Threads,
                           WideTile<BT>::Smem, s, mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W,
-                          p.err);
+                          early_w, p.err);
     return launch_pdl(mix_wide_kernel<BT, kMix>, grid, WideTile<BT>::Threads, WideTile<BT>::Smem,
-                      s, mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, p.err);
+                      s, mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, early_w, p.err);
 }
 
 // 3D tensor map over a complex64 array [d2][d1][NM] viewed as floats: dims
@@ -295,7 +301,8 @@ bool mix_wide_supported(int B, int Cin, int Cout, int nm) {
 }
 
 cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
-                            cudaStream_t s, fno_launch_ctx* ctx) {
+                            bool after_own_forward, cudaStream_t s, fno_launch_ctx* ctx) {
+    const int early_w = after_own_forward ? 1 : 0;
     const int bt = wide_bt(p.B);
     int ic = 0;
     switch (bt) {
@@ -314,11 +321,11 @@ cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* 
         return cudaErrorInvalidValue;
     cudaError_t e;
     switch (bt) {
-        case 1: e = launch_bt<1>(mw, mx, Z, p, s); break;
-        case 2: e = launch_bt<2>(mw, mx, Z, p, s); break;
-        case 4: e = launch_bt<4>(mw, mx, Z, p, s); break;
-        case 8: e = launch_bt<8>(mw, mx, Z, p, s); break;
-        default: e = launch_bt<16>(mw, mx, Z, p, s); break;
+        case 1: e = launch_bt<1>(mw, mx, Z, p, early_w, s); break;
+        case 2: e = launch_bt<2>(mw, mx, Z, p, early_w, s); break;
+        case 4: e = launch_bt<4>(mw, mx, Z, p, early_w, s); break;
+        case 8: e = launch_bt<8>(mw, mx, Z, p, early_w, s); break;
+        default: e = launch_bt<16>(mw, mx, Z, p, early_w, s); break;
     }
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
@@ -335,6 +342,7 @@ cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2
         return cudaErrorInvalidValue;
     const dim3 grid(((p.nm + kModes - 1) / kModes) * ((p.Cout + kOCB - 1) / kOCB), 1,
                     (p.Cin + 15) / 16);
+    // G comes from an earlier kernel than the forward stage just before this one
     return launch_pdl(mix_wide_kernel<16, kWgrad>, grid, T::Threads, T::Smem, s, mg, mx, gw,
-                      p.Cin, p.B, p.Cout, p.nm, p.m2, p.W, p.err);
+                      p.Cin, p.B, p.Cout, p.nm, p.m2, p.W, 1, p.err);
 }
