@@ -225,6 +225,35 @@ def spectral_conv2d_backward(x, w, g, m1: int, m2: int):
     return gx, gw
 
 
+def gelu(v) -> np.ndarray:
+    """GELU in its erf form, v * Phi(v) = v/2 * (1 + erf(v / sqrt(2))), in double."""
+    from scipy.special import erf
+    v = np.asarray(v, dtype=np.float64)
+    return 0.5 * v * (1.0 + erf(v / np.sqrt(2.0)))
+
+
+def pointwise(x, w_pw, bias=None) -> np.ndarray:
+    """The 1x1 convolution of the FNO block: out[b,o,h,w] = sum_i w_pw[o,i] x[b,i,h,w]
+    (+ bias[o]), in double."""
+    x = _real(x)
+    w_pw = _real(w_pw)
+    out = np.einsum("oi,bihw->bohw", w_pw, x)
+    if bias is not None:
+        out = out + _real(bias)[None, :, None, None]
+    return out
+
+
+def block(x, w, w_pw, bias, m1: int, m2: int, activation: str = "gelu") -> np.ndarray:
+    """One FNO block: act(spectral_conv2d(x, w) + w_pw x + bias), act in
+    {"gelu", "none"} (the spectral layer plus the pointwise branch and the
+    activation that follows it in the neural-operator block)."""
+    y = spectral_conv2d(x, w, m1, m2) + pointwise(x, w_pw, bias)
+    if activation == "gelu":
+        return gelu(y)
+    assert activation == "none"
+    return y
+
+
 def forward_modes_parallel(x, m1: int, m2: int, threads: int | None = None) -> np.ndarray:
     """forward_modes over independent planes on several host threads.
 

@@ -351,3 +351,48 @@ def test_mix_adjoint_and_weight_grad_match_numpy():
                        rtol=1e-12, atol=1e-12)
     assert np.allclose(oracle.weight_grad(X, G), np.einsum("bim,bom->iom", np.conj(X), G),
                        rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------ block epilogue ---
+
+def test_gelu_closed_forms():
+    import math
+    v = np.array([-3.0, -1.0, -0.25, 0.0, 0.5, 2.0, 6.0])
+    g = oracle.gelu(v)
+    # scalar definition with the standard library's erf (independent of scipy)
+    ref = np.array([0.5 * t * (1.0 + math.erf(t / math.sqrt(2.0))) for t in v])
+    assert np.allclose(g, ref, rtol=1e-15, atol=1e-15)
+    # Phi(t) + Phi(-t) = 1  =>  gelu(t) - gelu(-t) = t
+    t = RNG.standard_normal(1000) * 3
+    assert np.allclose(oracle.gelu(t) - oracle.gelu(-t), t, rtol=0, atol=1e-13)
+    assert oracle.gelu(0.0) == 0.0 and abs(oracle.gelu(40.0) - 40.0) < 1e-12
+
+
+def test_pointwise_brute_force():
+    B, Cin, Cout, H, W = 2, 3, 4, 5, 6
+    x = RNG.standard_normal((B, Cin, H, W))
+    wpw = RNG.standard_normal((Cout, Cin))
+    bias = RNG.standard_normal(Cout)
+    out = oracle.pointwise(x, wpw, bias)
+    for b in range(B):
+        for o in range(Cout):
+            for h in range(H):
+                for w_ in range(W):
+                    want = bias[o] + sum(wpw[o, i] * x[b, i, h, w_] for i in range(Cin))
+                    assert abs(out[b, o, h, w_] - want) < 1e-12
+
+
+def test_block_special_cases():
+    B, Cin, Cout, H, W, m1, m2 = 2, 3, 2, 8, 8, 2, 3
+    x = RNG.standard_normal((B, Cin, H, W))
+    w = rand_w(Cin, Cout, m1, m2)
+    zero_pw = np.zeros((Cout, Cin))
+    # no pointwise branch, no bias, no activation: the spectral layer itself
+    assert np.allclose(oracle.block(x, w, zero_pw, np.zeros(Cout), m1, m2, "none"),
+                       oracle.spectral_conv2d(x, w, m1, m2), rtol=1e-13, atol=1e-13)
+    # no spectral weights: the pointwise branch through GELU
+    wpw = RNG.standard_normal((Cout, Cin))
+    bias = RNG.standard_normal(Cout)
+    assert np.allclose(oracle.block(x, np.zeros_like(w), wpw, bias, m1, m2),
+                       oracle.gelu(np.einsum("oi,bihw->bohw", wpw, x) + bias[None, :, None, None]),
+                       rtol=1e-13, atol=1e-13)
