@@ -409,6 +409,92 @@ def run_ours(args, cfg):
         dist.destroy_process_group()
 
 
+def run_ours_block(args, cfg):
+    """Time fno_block_execute (spectral layer + pointwise branch + bias + GELU)
+    on the workload; one JSON line.  Algorithmic bytes: x read, y written, w and
+    w_pw read; flops: the mode contraction plus the pointwise branch
+    (2*B*Cin*Cout*H*W); roofline = max(bytes / HBM peak, flops / FP32 peak)."""
+    import torch
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__ as g
+    g.build()
+    from fourier_neural_spectral_gb300 import fnospec
+
+    peaks, peak_kind = read_peaks()
+    plan = fnospec.Plan(cfg.B, cfg.Cin, cfg.Cout, cfg.H, cfg.W, cfg.m1, cfg.m2)
+    step_bytes = cfg.algorithmic_bytes() + 4 * cfg.Cin * cfg.Cout
+    nsets = max(1, min(8, -(-3 * L2_BYTES // step_bytes) + 1)) if step_bytes < 3 * L2_BYTES else 1
+    x0, w0 = synth.make_inputs(cfg)
+    xs = [torch.from_numpy(x0).to(dev)]
+    for k in range(1, nsets):
+        xs.append(torch.roll(xs[0], shifts=k, dims=0).contiguous())
+    wt = torch.from_numpy(w0).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(0)
+    wpw = torch.randn((cfg.Cout, cfg.Cin), device=dev, generator=gen) / cfg.Cin ** 0.5
+    bias = torch.randn((cfg.Cout,), device=dev, generator=gen)
+    ys = [torch.empty((cfg.B, cfg.Cout, cfg.H, cfg.W), dtype=torch.float32, device=dev)
+          for _ in range(nsets)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        j = i % nsets
+        plan.fno_block_execute(xs[j], wt, wpw, bias, ys[j], "gelu", stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if plan.fno_get_device_status() != fnospec.FNO_OK:
+        raise RuntimeError("device status not clean after warm-up")
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    if plan.fno_get_device_status() != fnospec.FNO_OK:
+        raise RuntimeError("device status not clean after timed steps")
+    ms_per_step = elapsed_ms / args.steps
+    hbm = float(peaks["hbm_gbs"])
+    flops = cfg.gemm_flops() + 2 * cfg.B * cfg.Cin * cfg.Cout * cfg.H * cfg.W
+    fp32_peak = fp32_fma_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)))
+    t_roof = max(step_bytes / (hbm * 1e9), flops / (fp32_peak * 1e12))
+    if rank == 0:
+        cfgd = config_dict(cfg, "fp32")
+        cfgd["pass"] = "FNO block: gelu(layer(x, w) + w_pw x + bias)"
+        line = {
+            "metric": "FNO block samples/s", "value":
+                aggregate_value(world, cfg.B, args.steps, elapsed_ms),
+            "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfgd,
+            "layer_roofline": {"bytes_per_step": step_bytes, "flops_per_step": flops,
+                               "t_roof_us": t_roof * 1e6, "t_step_us": ms_per_step * 1e3,
+                               "frac": t_roof / (ms_per_step * 1e-3), "peak_gbs": hbm,
+                               "fp32_peak_tflops_at_max_clock": fp32_peak,
+                               "peak_kind": peak_kind},
+            "plan": plan.description, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_ours_backward(args, cfg):
     """Time fno_plan_backward (both gradients) on the workload; one JSON line.
 
@@ -502,8 +588,10 @@ def main():
     ap.add_argument("--precision", default="fp32", choices=["fp32", "tf32", "3xtf32"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
-                    help="forward (the headline) or the layer's backward (fp32)")
+    ap.add_argument("--pass", dest="pass_", default="forward",
+                    choices=["forward", "backward", "block"],
+                    help="forward (the headline), the layer's backward, or one FNO block "
+                         "(layer + pointwise branch + bias + GELU); fp32")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -512,6 +600,8 @@ def main():
         run_reference(args, cfg)
     elif args.pass_ == "backward":
         run_ours_backward(args, cfg)
+    elif args.pass_ == "block":
+        run_ours_block(args, cfg)
     else:
         run_ours(args, cfg)
 

@@ -192,6 +192,7 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
         if (g_init_err == cudaSuccess) g_init_err = mix_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_tma_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_wide_init();
+        if (g_init_err == cudaSuccess) g_init_err = block_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_tc_init();
     });
     if (g_init_err != cudaSuccess) return FNO_ERR_CUDA;
@@ -418,6 +419,49 @@ fno_status_t fno_plan_execute(fno_plan_t p, const float* x, const void* w, float
     if (e == cudaSuccess) e = run_mix(*p, X, static_cast<const float2*>(w), Z, s, &ctx, true);
     if (e == cudaSuccess) e = run_inverse(*p, Z, y, T, s, &ctx);
     return cuda_status(e);
+}
+
+namespace {
+
+fno_status_t check_block_args(const fno_plan_s* p, const float* x, const float* w_pw,
+                              const float* bias, fno_activation_t act, const float* y) {
+    fno_status_t st;
+    if ((st = check_device(p)) != FNO_OK) return st;
+    if (act != FNO_ACT_NONE && act != FNO_ACT_GELU) return FNO_ERR_INVALID_ARG;
+    if (!block_supported(p->Cin)) return FNO_ERR_UNSUPPORTED;
+    if ((st = check_ptr(x, true)) != FNO_OK) return st;
+    if ((st = check_ptr(w_pw, true)) != FNO_OK) return st;
+    if ((st = check_ptr(bias, false)) != FNO_OK) return st;
+    if ((st = check_ptr(y, true)) != FNO_OK) return st;
+    const size_t wpw_bytes = 4ull * p->Cin * p->Cout, bias_bytes = 4ull * p->Cout;
+    if (overlaps(y, y_bytes(p), x, x_bytes(p)) || overlaps(y, y_bytes(p), w_pw, wpw_bytes) ||
+        (bias && overlaps(y, y_bytes(p), bias, bias_bytes)))
+        return FNO_ERR_INVALID_ARG;
+    return FNO_OK;
+}
+
+}  // namespace
+
+fno_status_t fno_block_epilogue(fno_plan_t p, const float* x, const float* w_pw, const float* bias,
+                                fno_activation_t act, float* y, cudaStream_t s) {
+    if (!p) return FNO_ERR_INVALID_ARG;
+    fno_status_t st = check_block_args(p, x, w_pw, bias, act, y);
+    if (st != FNO_OK) return st;
+    return cuda_status(launch_block_epilogue(*p, x, w_pw, bias, (int)act, y, false, s));
+}
+
+fno_status_t fno_block_execute(fno_plan_t p, const float* x, const void* w, const float* w_pw,
+                               const float* bias, fno_activation_t act, float* y, void* ws,
+                               size_t ws_bytes, cudaStream_t s) {
+    if (!p) return FNO_ERR_INVALID_ARG;
+    fno_status_t st = check_block_args(p, x, w_pw, bias, act, y);
+    if (st != FNO_OK) return st;
+    st = fno_plan_execute(p, x, w, y, ws, ws_bytes, s);
+    if (st != FNO_OK) return st;
+    // the kernel just before is the plan's own inverse stage (launched either with
+    // programmatic serialisation, after its own wait, or normally), so w_pw and
+    // bias may be read before the epilogue's launch wait
+    return cuda_status(launch_block_epilogue(*p, x, w_pw, bias, (int)act, y, true, s));
 }
 
 fno_status_t fno_forward_modes(fno_plan_t p, const float* x, void* X, void* ws, size_t ws_bytes,

@@ -115,6 +115,13 @@ cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* 
 cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2* G, float2* gw,
                               cudaStream_t s);
 
+// FNO block epilogue (block.cu).
+cudaError_t block_init();
+bool block_supported(int Cin);
+cudaError_t launch_block_epilogue(const fno_plan_s& p, const float* x, const float* w_pw,
+                                  const float* bias, int act, float* y, bool after_own_inverse,
+                                  cudaStream_t s);
+
 // Backward-only kernels (backward.cu).
 cudaError_t launch_wgrad(const float2* X, const float2* G, float2* gw, int B, int Cin, int Cout,
                          int nm, int m2, int W, cudaStream_t s);

@@ -27,6 +27,9 @@ FNO_ERR_DEVICE = 6
 FNO_PREC_FP32 = 0
 FNO_PREC_TF32 = 1
 FNO_PREC_3XTF32 = 2
+FNO_ACT_NONE = 0
+FNO_ACT_GELU = 1
+ACTIVATIONS = {"none": FNO_ACT_NONE, "gelu": FNO_ACT_GELU}
 PRECISIONS = {"fp32": FNO_PREC_FP32, "tf32": FNO_PREC_TF32, "3xtf32": FNO_PREC_3XTF32}
 
 # Every symbol include/fnospec.h declares.
@@ -35,6 +38,7 @@ EXPORTS = (
     "fno_plan_describe", "fno_plan_kernel_info", "fno_plan_record_events", "fno_plan_execute", "fno_plan_destroy", "fno_spectral_conv2d",
     "fno_release_cache", "fno_forward_modes", "fno_mix_modes", "fno_inverse_modes",
     "fno_get_device_status", "fno_spectral_conv2d_noalloc", "fno_plan_backward",
+    "fno_block_epilogue", "fno_block_execute",
 )
 
 
@@ -80,6 +84,8 @@ def load_library(path: str = LIB_PATH):
             "fno_get_device_status": (st, [vp, vp]),
             "fno_spectral_conv2d_noalloc": (st, [vp, vp, vp, i, i, i, i, i, i, i, vp]),
             "fno_plan_backward": (st, [vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "fno_block_epilogue": (st, [vp, vp, vp, vp, i, vp, vp]),
+            "fno_block_execute": (st, [vp, vp, vp, vp, vp, i, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -194,6 +200,23 @@ class Plan:
         wp, wn = self._ws(workspace)
         _check(load_library().fno_inverse_modes(self._h, _ptr(Z), _ptr(y), wp, wn,
                                                 _stream(stream)), "fno_inverse_modes")
+        return y
+
+    def fno_block_epilogue(self, x, w_pw, bias, y, activation="gelu", stream=None):
+        """y <- act(y + w_pw x + bias) in place (y: the spectral layer's output)."""
+        act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
+        _check(load_library().fno_block_epilogue(self._h, _ptr(x), _ptr(w_pw), _ptr(bias), act,
+                                                 _ptr(y), _stream(stream)), "fno_block_epilogue")
+        return y
+
+    def fno_block_execute(self, x, w, w_pw, bias, y, activation="gelu", workspace=None,
+                          stream=None):
+        """One FNO block: y = act(layer(x, w) + w_pw x + bias)."""
+        act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
+        wp, wn = self._ws(workspace)
+        _check(load_library().fno_block_execute(self._h, _ptr(x), _weight_ptr(w), _ptr(w_pw),
+                                                _ptr(bias), act, _ptr(y), wp, wn,
+                                                _stream(stream)), "fno_block_execute")
         return y
 
     def fno_plan_backward(self, x, w, gy, gx=None, gw=None, workspace=None, stream=None):

@@ -114,6 +114,33 @@ fno_status_t fno_plan_record_events(fno_plan_t plan, cudaEvent_t* events, int co
 fno_status_t fno_plan_execute(fno_plan_t plan, const float* x, const void* w, float* y,
                               void* workspace, size_t workspace_bytes, cudaStream_t s);
 
+/* Activation of the FNO block (fno_block_execute / fno_block_epilogue). */
+typedef enum {
+    FNO_ACT_NONE = 0, /* identity */
+    FNO_ACT_GELU = 1  /* v/2 * (1 + erf(v / sqrt(2))), erf from the CUDA math library */
+} fno_activation_t;
+
+/* The FNO block around the spectral layer, in place over y:
+ *   y[b][o][h][w] <- act(y[b][o][h][w] + bias[o] + sum_i w_pw[o][i] * x[b][i][h][w])
+ * with y on entry the spectral layer's output for x (fno_plan_execute), w_pw the
+ * 1x1 convolution weights float [Cout][Cin] (PyTorch's [Cout, Cin, 1, 1]), bias
+ * float [Cout] or NULL (no bias).  This is the pointwise branch and activation
+ * that the neural-operator block adds to the spectral path (the FFT operator-
+ * optimisation page, section 5.2, fuses such a branch-add and GELU into the
+ * last stage of its FFT convolution).  Needs Cin <= 256 (FNO_ERR_UNSUPPORTED
+ * otherwise).  y must not overlap x, w_pw or bias.  Stream-ordered, no host
+ * synchronisation, no allocation. */
+fno_status_t fno_block_epilogue(fno_plan_t plan, const float* x, const float* w_pw,
+                                const float* bias, fno_activation_t act, float* y,
+                                cudaStream_t s);
+
+/* fno_plan_execute followed by fno_block_epilogue: one FNO block
+ *   y = act(layer(x, w) + w_pw x + bias)
+ * with the plan's workspace (fno_plan_workspace_size bytes). */
+fno_status_t fno_block_execute(fno_plan_t plan, const float* x, const void* w, const float* w_pw,
+                               const float* bias, fno_activation_t act, float* y,
+                               void* workspace, size_t workspace_bytes, cudaStream_t s);
+
 /* Backward of the layer for a real loss L, given gy = dL/dy (float
  * [B][Cout][H][W]), on stream s:
  *   gx = dL/dx, float [B][Cin][H][W]: the layer applied to gy with w conjugated
