@@ -15,16 +15,14 @@ namespace {
 
 constexpr int kMaxN = 4096;
 
-bool is_pow2(int v) { return v >= 1 && (v & (v - 1)) == 0; }
-
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 fno_status_t validate_shape(int B, int Cin, int Cout, int H, int W, int m1, int m2) {
     if (B < 1 || Cin < 1 || Cout < 1 || H < 1 || W < 1 || m1 < 1 || m2 < 1)
         return FNO_ERR_INVALID_ARG;
     if (2LL * m1 > H || (long long)m2 > W / 2 + 1) return FNO_ERR_INVALID_ARG;
-    if (!is_pow2(H) || !is_pow2(W) || H < 2 || W < 2 || H > kMaxN || W > kMaxN)
-        return FNO_ERR_UNSUPPORTED;
+    // powers of two run on the FFT kernels, other sizes on direct DFTs
+    if (H < 2 || W < 2 || H > kMaxN || W > kMaxN) return FNO_ERR_UNSUPPORTED;
     const long long lim = (1LL << 31) - 1;
     if ((long long)B * Cin * H * W > lim || (long long)B * Cout * H * W > lim ||
         (long long)Cin * Cout * 2 * m1 * m2 > lim)
@@ -187,6 +185,7 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
 
     std::call_once(g_init_once, [] {
         g_init_err = stages_generic_init();
+        if (g_init_err == cudaSuccess) g_init_err = stages_dft_init();
         if (g_init_err == cudaSuccess) g_init_err = stages_fused_init();
         if (g_init_err == cudaSuccess) g_init_err = stages_big_init();
         if (g_init_err == cudaSuccess) g_init_err = mix_init();
@@ -261,6 +260,14 @@ fno_plan_s* plan_new(int B, int Cin, int Cout, int H, int W, int m1, int m2,
         std::snprintf(p->desc, sizeof(p->desc),
                       "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|%s|inv-cols+rows(R=%d,P=%d)", W,
                       p->R, p->P, mix_name(p), p->Ri, p->Pi);
+    } else if (dft_path(H, W)) {
+        describe_generic(p);
+        std::snprintf(p->kernels[0].name, sizeof(p->kernels[0].name), "dft_rows");
+        std::snprintf(p->kernels[1].name, sizeof(p->kernels[1].name), "dft_cols");
+        std::snprintf(p->kernels[3].name, sizeof(p->kernels[3].name), "dft_icols");
+        std::snprintf(p->kernels[4].name, sizeof(p->kernels[4].name), "dft_irows");
+        std::snprintf(p->desc, sizeof(p->desc),
+                      "direct-dft: rows(W=%d)|cols(H=%d)|%s|icols|irows", W, H, mix_name(p));
     } else {
         describe_generic(p);
         std::snprintf(p->desc, sizeof(p->desc),
@@ -428,7 +435,7 @@ fno_status_t check_block_args(const fno_plan_s* p, const float* x, const float* 
     fno_status_t st;
     if ((st = check_device(p)) != FNO_OK) return st;
     if (act != FNO_ACT_NONE && act != FNO_ACT_GELU) return FNO_ERR_INVALID_ARG;
-    if (!block_supported(p->Cin)) return FNO_ERR_UNSUPPORTED;
+    if (!block_supported(p->Cin) || (p->H * p->W) % 4 != 0) return FNO_ERR_UNSUPPORTED;
     if ((st = check_ptr(x, true)) != FNO_OK) return st;
     if ((st = check_ptr(w_pw, true)) != FNO_OK) return st;
     if ((st = check_ptr(bias, false)) != FNO_OK) return st;

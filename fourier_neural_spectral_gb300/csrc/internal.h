@@ -134,6 +134,15 @@ bool mix_tc_supported(int B, int Cin, int Cout, int nm, int split);
 cudaError_t launch_mix_tc(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                           int split, cudaStream_t s, fno_launch_ctx* ctx);
 
+// Direct-DFT transforms for H or W not a power of two (stages_dft.cu); the
+// shape-generic launchers below route such shapes there.
+bool dft_path(int H, int W);
+cudaError_t stages_dft_init();
+cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, float2* T,
+                               cudaStream_t s, fno_launch_ctx* ctx);
+cudaError_t launch_inverse_dft(const fno_plan_s& p, const float2* Z, float* y, float2* T,
+                               cudaStream_t s, fno_launch_ctx* ctx);
+
 // Stage launchers (all asynchronous on stream s).
 // Each launcher calls ctx->mark(s) after every kernel it enqueues.
 cudaError_t launch_forward_modes(const fno_plan_s& p, const float* x, float2* X, float2* T,

@@ -184,6 +184,7 @@ cudaError_t stages_generic_init() {
 
 cudaError_t launch_forward_modes(const fno_plan_s& p, const float* x, float2* X, float2* T,
                                  cudaStream_t s, fno_launch_ctx* ctx) {
+    if (dft_path(p.H, p.W)) return launch_forward_dft(p, x, X, T, s, ctx);
     const long long npairs = (long long)p.B * p.Cin * p.H / 2;
     {
         const int S = seqs_for(p.W);
@@ -208,6 +209,7 @@ cudaError_t launch_forward_modes(const fno_plan_s& p, const float* x, float2* X,
 
 cudaError_t launch_inverse_modes(const fno_plan_s& p, const float2* Z, float* y, float2* T,
                                  cudaStream_t s, fno_launch_ctx* ctx) {
+    if (dft_path(p.H, p.W)) return launch_inverse_dft(p, Z, y, T, s, ctx);
     {
         const int S = std::min(seqs_for(p.H), p.m2);
         const size_t smem = 2 * sizeof(float2) * (size_t)S * p.H;

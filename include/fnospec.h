@@ -30,7 +30,8 @@
  *   - Work is enqueued on the given stream and returns without synchronising
  *     and without allocating (except the one-shot fno_spectral_conv2d, which
  *     caches a plan and a workspace on its first call per shape and stream).
- *   - Supported shapes: H and W powers of two in [2, 4096]; 1 <= m1, 2*m1 <= H;
+ *   - Supported shapes: H and W in [2, 4096] (powers of two run on FFT kernels,
+ *     other sizes on direct DFTs of the retained bins); 1 <= m1, 2*m1 <= H;
  *     1 <= m2 <= W/2 + 1; B, Cin, Cout >= 1; every tensor below 2^31 elements.
  *   - Errors detected on the host are returned immediately and nothing is
  *     enqueued.  Errors detected inside kernels set a word in device memory
@@ -127,8 +128,8 @@ typedef enum {
  * float [Cout] or NULL (no bias).  This is the pointwise branch and activation
  * that the neural-operator block adds to the spectral path (the FFT operator-
  * optimisation page, section 5.2, fuses such a branch-add and GELU into the
- * last stage of its FFT convolution).  Needs Cin <= 256 (FNO_ERR_UNSUPPORTED
- * otherwise).  y must not overlap x, w_pw or bias.  Stream-ordered, no host
+ * last stage of its FFT convolution).  Needs Cin <= 256 and H*W a multiple of
+ * 4 (FNO_ERR_UNSUPPORTED otherwise).  y must not overlap x, w_pw or bias.  Stream-ordered, no host
  * synchronisation, no allocation. */
 fno_status_t fno_block_epilogue(fno_plan_t plan, const float* x, const float* w_pw,
                                 const float* bias, fno_activation_t act, float* y,

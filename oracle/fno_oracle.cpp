@@ -87,11 +87,8 @@ inline long long row_of(long long r, long long H, long long m1) {
     return r < m1 ? r : H - 2 * m1 + r;
 }
 
-bool pow2(long long v) { return v >= 1 && (v & (v - 1)) == 0; }
-
 bool shape_ok(int B, int C, int H, int W, int m1, int m2) {
     if (B <= 0 || C <= 0 || H < 2 || W < 2 || m1 <= 0 || m2 <= 0) return false;
-    if (!pow2(H) || !pow2(W)) return false;
     if (2 * (long long)m1 > H) return false;
     if ((long long)m2 > W / 2 + 1) return false;
     return true;

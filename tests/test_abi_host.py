@@ -48,7 +48,7 @@ def test_status_strings(lib):
     ((2, 4, 4, 16, 16, 9, 4), 1),     # 2*m1 > H
     ((2, 4, 4, 16, 16, 4, 10), 1),    # m2 > W/2 + 1
     ((2, 4, 4, 16, 16, 0, 4), 1),     # m1 = 0
-    ((2, 4, 4, 24, 16, 4, 4), 2),     # H not a power of two
+    ((2, 4, 4, 8192, 16, 4, 4), 2),   # H above 4096
     ((2, 4, 4, 16, 8192, 4, 4), 2),   # W above 4096
     ((2, 4, 4, 1, 16, 0, 4), 1),      # H = 1 (m1 must be >= 1)
 ])

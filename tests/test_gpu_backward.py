@@ -27,6 +27,7 @@ BACKWARD_SHAPES = [
     (1, 4, 4, 256, 256, 64, 64),    # 256-point rows
     (1, 2, 3, 512, 2048, 64, 16),   # long rows, row groups (P > 1), staged Z
     (2, 3, 2, 1024, 64, 100, 7),    # m1 > R: several frequencies per residue
+    (2, 3, 4, 24, 20, 5, 6),        # not powers of two: direct-DFT transforms
 ]
 
 

@@ -40,6 +40,13 @@ EDGE_SHAPES = [
     (5, 19, 13, 64, 64, 9, 11),     # nm = 198, Cout % 8 != 0, B = 5, Cin % IC != 0
     (20, 7, 9, 32, 64, 4, 9),       # B > 16: two batch tiles, nm = 72
     (1, 3, 2, 64, 32, 8, 2),        # B = 1, nm = 32 exactly
+    # sizes that are not powers of two: direct-DFT transforms
+    (2, 3, 4, 24, 16, 4, 4),        # H = 24
+    (1, 2, 2, 421, 421, 12, 12),    # 421 x 421 (the Darcy-flow grid of the FNO literature)
+    (3, 5, 7, 85, 85, 16, 16),      # odd sizes, 2*m1*m2 = 512 modes
+    (2, 2, 3, 30, 50, 15, 26),      # 2*m1 = H, Nyquist column kept
+    (1, 1, 1, 3, 5, 1, 3),          # smallest odd grid
+    (1, 2, 2, 100, 4096, 10, 20),   # long power-of-two rows with H = 100
     # long rows (three-level row transform, shuffle reduce-scatter)
     (2, 3, 4, 64, 512, 16, 33),     # W = 512
     (1, 2, 2, 32, 1024, 8, 64),     # W = 1024, the largest supported m2

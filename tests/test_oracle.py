@@ -255,7 +255,7 @@ def test_truncation_is_not_idempotent():
 
 
 @pytest.mark.parametrize("args", [
-    (0, 1, 8, 8, 2, 2), (1, 1, 8, 8, 5, 2), (1, 1, 8, 8, 2, 6), (1, 1, 12, 8, 2, 2),
+    (0, 1, 8, 8, 2, 2), (1, 1, 8, 8, 5, 2), (1, 1, 8, 8, 2, 6), (1, 1, 12, 8, 7, 2),
     (1, 1, 8, 8, 0, 2), (1, 1, 1, 8, 1, 2)])
 def test_invalid_shapes_rejected(args):
     B, C, H, W, m1, m2 = args
@@ -396,3 +396,17 @@ def test_block_special_cases():
     assert np.allclose(oracle.block(x, np.zeros_like(w), wpw, bias, m1, m2),
                        oracle.gelu(np.einsum("oi,bihw->bohw", wpw, x) + bias[None, :, None, None]),
                        rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("B,Cin,Cout,H,W,m1,m2", [
+    (1, 2, 3, 12, 10, 3, 4),     # neither a power of two, even W (Nyquist at 5)
+    (2, 1, 2, 9, 7, 2, 4),       # odd H and W (no Nyquist column)
+    (1, 2, 2, 30, 50, 15, 26),   # 2*m1 = H, m2 = W/2 + 1
+    (1, 1, 1, 3, 5, 1, 3),       # smallest odd grid, every column kept
+])
+def test_layer_matches_numpy_any_size(B, Cin, Cout, H, W, m1, m2):
+    # the layer's definition holds for any H, W; numpy's pocketfft is independent
+    x = RNG.standard_normal((B, Cin, H, W))
+    w = rand_w(Cin, Cout, m1, m2)
+    assert np.allclose(oracle.spectral_conv2d(x, w, m1, m2), numpy_layer(x, w, m1, m2),
+                       rtol=1e-11, atol=1e-11)
