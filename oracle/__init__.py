@@ -225,6 +225,56 @@ def spectral_conv2d_backward(x, w, g, m1: int, m2: int):
     return gx, gw
 
 
+def _roots(L: int, sign: int) -> np.ndarray:
+    """exp(sign * 2 pi i j / L) for j in [0, L), angles from the exact integer j."""
+    j = np.arange(L, dtype=np.float64)
+    return np.exp(sign * 2j * np.pi * j / L)
+
+
+def spectral_conv1d(x, w, m: int) -> np.ndarray:
+    """The 1D layer in double, by direct sums:
+      X[b,i,k] = 1/sqrt(L) sum_n x[b,i,n] exp(-2 pi i k n / L),   k < m
+      Z[b,o,k] = sum_i X[b,i,k] w[i,o,k]
+      y[b,o,n] = 1/sqrt(L) sum_{k<m} c(k) Re(Z[b,o,k] exp(+2 pi i k n / L))
+    with c = 1 for k = 0 and k = L/2, else 2 (the irfft of the truncated half
+    spectrum, norm="ortho")."""
+    x = _real(x)
+    w = np.asarray(w, dtype=np.complex128)
+    B, Cin, L = x.shape
+    assert w.shape[0] == Cin and w.shape[2] == m and 1 <= m <= L // 2 + 1
+    k = np.arange(m)
+    n = np.arange(L)
+    kn = np.outer(k, n) % L                        # exact integer products, reduced
+    F = _roots(L, -1)[kn] / np.sqrt(L)             # [m, L]
+    X = np.einsum("bin,kn->bik", x, F)
+    Z = np.einsum("bik,iok->bok", X, w)
+    c = np.where((k == 0) | (2 * k == L), 1.0, 2.0)
+    G = _roots(L, +1)[kn] / np.sqrt(L)             # [m, L]
+    return np.real(np.einsum("bok,kn->bon", Z * c, G))
+
+
+def spectral_conv1d_backward(x, w, g, m: int):
+    """(gx, gw) of the 1D layer for dL/dy = g, by the same derivation as the 2D
+    backward: dL/dZ = c(k) G with G the truncated DFT of g; dL/dx is the
+    transpose of the truncated DFT applied to sum_o dL/dZ conj(w); dL/dw =
+    sum_b conj(X) dL/dZ."""
+    x = _real(x)
+    g = _real(g)
+    w = np.asarray(w, dtype=np.complex128)
+    B, Cin, L = x.shape
+    k = np.arange(m)
+    n = np.arange(L)
+    kn = np.outer(k, n) % L
+    F = _roots(L, -1)[kn] / np.sqrt(L)
+    c = np.where((k == 0) | (2 * k == L), 1.0, 2.0)
+    X = np.einsum("bin,kn->bik", x, F)
+    GZ = np.einsum("bon,kn->bok", g, F) * c
+    GX = np.einsum("bok,iok->bik", GZ, np.conj(w))
+    gx = np.real(np.einsum("bik,kn->bin", GX, _roots(L, +1)[kn] / np.sqrt(L)))
+    gw = np.einsum("bik,bok->iok", np.conj(X), GZ)
+    return gx, gw
+
+
 def gelu(v) -> np.ndarray:
     """GELU in its erf form, v * Phi(v) = v/2 * (1 + erf(v / sqrt(2))), in double."""
     from scipy.special import erf

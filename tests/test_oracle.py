@@ -410,3 +410,51 @@ def test_layer_matches_numpy_any_size(B, Cin, Cout, H, W, m1, m2):
     w = rand_w(Cin, Cout, m1, m2)
     assert np.allclose(oracle.spectral_conv2d(x, w, m1, m2), numpy_layer(x, w, m1, m2),
                        rtol=1e-11, atol=1e-11)
+
+
+# -------------------------------------------------------------------- 1D ---
+
+def numpy_layer_1d(x, w, m):
+    """The 1D layer through numpy's FFT library (independent of the oracle)."""
+    B, Cin, L = x.shape
+    F = np.fft.rfft(x, norm="ortho")[:, :, :m]
+    Z = np.einsum("bik,iok->bok", F, w)
+    full = np.zeros((B, w.shape[1], L // 2 + 1), dtype=complex)
+    full[:, :, :m] = Z
+    return np.fft.irfft(full, n=L, norm="ortho")
+
+
+@pytest.mark.parametrize("B,Cin,Cout,L,m", [
+    (2, 3, 2, 16, 5), (1, 2, 2, 16, 9),   # Nyquist kept (m = L/2 + 1)
+    (2, 1, 3, 15, 8), (1, 2, 1, 100, 12),  # odd and non-power-of-two lengths
+])
+def test_layer_1d_matches_numpy(B, Cin, Cout, L, m):
+    x = RNG.standard_normal((B, Cin, L))
+    w = RNG.standard_normal((Cin, Cout, m)) + 1j * RNG.standard_normal((Cin, Cout, m))
+    assert np.allclose(oracle.spectral_conv1d(x, w, m), numpy_layer_1d(x, w, m),
+                       rtol=1e-12, atol=1e-12)
+
+
+def test_layer_1d_convolution_theorem():
+    # all modes kept, Cin = Cout = 1, w = unnormalised DFT of g: circular convolution
+    L = 12
+    x = RNG.standard_normal((1, 1, L))
+    g = RNG.standard_normal(L)
+    w = np.fft.rfft(g)[None, None, :]
+    y = oracle.spectral_conv1d(x, w, L // 2 + 1)
+    ref = np.array([sum(x[0, 0, j] * g[(n - j) % L] for j in range(L)) for n in range(L)])
+    assert np.allclose(y[0, 0], ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("L,m", [(16, 9), (15, 6)])
+def test_backward_1d_identities(L, m):
+    B, Cin, Cout = 2, 3, 2
+    x = RNG.standard_normal((B, Cin, L))
+    g = RNG.standard_normal((B, Cout, L))
+    w = RNG.standard_normal((Cin, Cout, m)) + 1j * RNG.standard_normal((Cin, Cout, m))
+    v = RNG.standard_normal((Cin, Cout, m)) + 1j * RNG.standard_normal((Cin, Cout, m))
+    gx, gw = oracle.spectral_conv1d_backward(x, w, g, m)
+    lhs = np.sum(oracle.spectral_conv1d(x, w, m) * g)
+    assert abs(lhs - np.sum(x * gx)) <= 1e-12 * np.abs(x * gx).sum()
+    lhs = np.sum(oracle.spectral_conv1d(x, v, m) * g)
+    assert abs(lhs - np.real(np.sum(np.conj(gw) * v))) <= 1e-12 * np.abs(np.conj(gw) * v).sum()
