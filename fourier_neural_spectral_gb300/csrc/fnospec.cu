@@ -32,6 +32,17 @@ fno_status_t validate_shape(int B, int Cin, int Cout, int H, int W, int m1, int 
     return FNO_OK;
 }
 
+fno_status_t validate_shape_1d(int B, int Cin, int Cout, int L, int m) {
+    if (B < 1 || Cin < 1 || Cout < 1 || L < 1 || m < 1) return FNO_ERR_INVALID_ARG;
+    if ((long long)m > L / 2 + 1) return FNO_ERR_INVALID_ARG;
+    if (L < 2 || L > kMaxN) return FNO_ERR_UNSUPPORTED;
+    const long long lim = (1LL << 31) - 1;
+    if ((long long)B * Cin * L > lim || (long long)B * Cout * L > lim ||
+        (long long)Cin * Cout * m > lim)
+        return FNO_ERR_UNSUPPORTED;
+    return FNO_OK;
+}
+
 // A pointer the kernels can dereference: device or managed memory, or host
 // memory that is registered/pinned and mapped (the GPU reaches it through UVA).
 // Unregistered host memory would fault the GPU, so it is rejected here.
@@ -126,13 +137,25 @@ void describe_fused(fno_plan_s* p) {
     p->launches = k;
 }
 
+// Kernel list of the 1D layer (stages_dft.cu row transforms + a contraction).
+void describe_1d(fno_plan_s* p) {
+    const size_t Pi = (size_t)p->B * p->Cin, Po = (size_t)p->B * p->Cout;
+    set_kernel(p, 0, "dft1_fwd", x_bytes(p) + X_bytes(p), 8ull * Pi * p->W * p->m2);
+    set_kernel(p, 1, mix_name(p), X_bytes(p) + w_bytes(p) + Z_bytes(p),
+               8ull * p->B * p->Cin * p->Cout * p->nm);
+    set_kernel(p, 2, "dft1_inv", Z_bytes(p) + y_bytes(p), 4ull * Po * p->W * p->m2);
+    p->launches = 3;
+}
+
 cudaError_t run_forward(const fno_plan_s& p, const float* x, float2* X, float2* T, cudaStream_t s,
                         fno_launch_ctx* ctx) {
+    if (p.dims == 1) return launch_forward_1d(p, x, X, s, ctx);
     return p.path == 1 ? launch_forward_fused(p, x, X, s, ctx) : launch_forward_modes(p, x, X, T, s, ctx);
 }
 
 cudaError_t run_inverse(const fno_plan_s& p, const float2* Z, float* y, float2* T, cudaStream_t s,
                         fno_launch_ctx* ctx) {
+    if (p.dims == 1) return launch_inverse_1d(p, Z, y, s, ctx);
     return p.path == 1 ? launch_inverse_fused(p, Z, y, s, ctx) : launch_inverse_modes(p, Z, y, T, s, ctx);
 }
 
@@ -154,8 +177,41 @@ fno_status_t cuda_status(cudaError_t e) {
 std::once_flag g_init_once;
 cudaError_t g_init_err = cudaSuccess;
 
-fno_plan_s* plan_new(int B, int Cin, int Cout, int H, int W, int m1, int m2,
+fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, int m2,
                      fno_precision_t prec, fno_plan_s* parent);
+
+cudaError_t init_once() {
+    std::call_once(g_init_once, [] {
+        g_init_err = stages_generic_init();
+        if (g_init_err == cudaSuccess) g_init_err = stages_dft_init();
+        if (g_init_err == cudaSuccess) g_init_err = stages_fused_init();
+        if (g_init_err == cudaSuccess) g_init_err = stages_big_init();
+        if (g_init_err == cudaSuccess) g_init_err = mix_init();
+        if (g_init_err == cudaSuccess) g_init_err = mix_tma_init();
+        if (g_init_err == cudaSuccess) g_init_err = mix_wide_init();
+        if (g_init_err == cudaSuccess) g_init_err = block_init();
+        if (g_init_err == cudaSuccess) g_init_err = mix_tc_init();
+    });
+    return g_init_err;
+}
+
+// A plan and its adjoint (the backward's plan: channels swapped, contraction
+// with w conjugated and transposed, tables and error word shared).
+fno_status_t plan_pair(fno_plan_t* out, int dims, int B, int Cin, int Cout, int H, int W, int m1,
+                       int m2, fno_precision_t prec) {
+    if (prec != FNO_PREC_FP32 && prec != FNO_PREC_TF32 && prec != FNO_PREC_3XTF32)
+        return FNO_ERR_INVALID_ARG;
+    if (init_once() != cudaSuccess) return FNO_ERR_CUDA;
+    fno_plan_s* p = plan_new(dims, B, Cin, Cout, H, W, m1, m2, prec, nullptr);
+    if (!p) return FNO_ERR_CUDA;
+    p->adj = plan_new(dims, B, Cout, Cin, H, W, m1, m2, FNO_PREC_FP32, p);
+    if (!p->adj) {
+        fno_plan_destroy(p);
+        return FNO_ERR_CUDA;
+    }
+    *out = p;
+    return FNO_OK;
+}
 
 }  // namespace
 
@@ -180,33 +236,16 @@ fno_status_t fno_plan_create(fno_plan_t* out, int B, int Cin, int Cout, int H, i
     *out = nullptr;
     fno_status_t st = validate_shape(B, Cin, Cout, H, W, m1, m2);
     if (st != FNO_OK) return st;
-    if (prec != FNO_PREC_FP32 && prec != FNO_PREC_TF32 && prec != FNO_PREC_3XTF32)
-        return FNO_ERR_INVALID_ARG;
+    return plan_pair(out, 2, B, Cin, Cout, H, W, m1, m2, prec);
+}
 
-    std::call_once(g_init_once, [] {
-        g_init_err = stages_generic_init();
-        if (g_init_err == cudaSuccess) g_init_err = stages_dft_init();
-        if (g_init_err == cudaSuccess) g_init_err = stages_fused_init();
-        if (g_init_err == cudaSuccess) g_init_err = stages_big_init();
-        if (g_init_err == cudaSuccess) g_init_err = mix_init();
-        if (g_init_err == cudaSuccess) g_init_err = mix_tma_init();
-        if (g_init_err == cudaSuccess) g_init_err = mix_wide_init();
-        if (g_init_err == cudaSuccess) g_init_err = block_init();
-        if (g_init_err == cudaSuccess) g_init_err = mix_tc_init();
-    });
-    if (g_init_err != cudaSuccess) return FNO_ERR_CUDA;
-
-    fno_plan_s* p = plan_new(B, Cin, Cout, H, W, m1, m2, prec, nullptr);
-    if (!p) return FNO_ERR_CUDA;
-    // the backward's plan: channels swapped, contraction with w conjugated and
-    // transposed, tables and error word shared with this plan
-    p->adj = plan_new(B, Cout, Cin, H, W, m1, m2, FNO_PREC_FP32, p);
-    if (!p->adj) {
-        fno_plan_destroy(p);
-        return FNO_ERR_CUDA;
-    }
-    *out = p;
-    return FNO_OK;
+fno_status_t fno_plan_create_1d(fno_plan_t* out, int B, int Cin, int Cout, int L, int m,
+                                fno_precision_t prec) {
+    if (!out) return FNO_ERR_INVALID_ARG;
+    *out = nullptr;
+    fno_status_t st = validate_shape_1d(B, Cin, Cout, L, m);
+    if (st != FNO_OK) return st;
+    return plan_pair(out, 1, B, Cin, Cout, 1, L, 0, m, prec);
 }
 
 }  // extern "C"
@@ -215,20 +254,22 @@ namespace {
 
 // A plan for (B, Cin, Cout, ...).  With a parent, it is that plan's adjoint:
 // the parent's tables and error word are shared and the contraction is the
-// conjugate-transpose one (fp32).  Returns nullptr on a CUDA error.
-fno_plan_s* plan_new(int B, int Cin, int Cout, int H, int W, int m1, int m2,
+// conjugate-transpose one (fp32).  dims = 1 is the 1D layer over W = L points
+// with m2 = m modes (H = 1, m1 = 0).  Returns nullptr on a CUDA error.
+fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, int m2,
                      fno_precision_t prec, fno_plan_s* parent) {
     fno_plan_s* p = new fno_plan_s();
     std::memset(p, 0, sizeof(*p));
+    p->dims = dims;
     p->B = B; p->Cin = Cin; p->Cout = Cout; p->H = H; p->W = W; p->m1 = m1; p->m2 = m2;
     p->adjoint = parent != nullptr;
-    p->nm = 2 * m1 * m2;
+    p->nm = dims == 1 ? m2 : 2 * m1 * m2;
     p->prec = prec;
     p->scale = (float)(1.0 / std::sqrt((double)H * (double)W));
     if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return nullptr; }
 
     int Rf = 0, Ri = 0;
-    p->path = fused_supported(W, H, m1, m2, &Rf, &Ri) ? 1 : 0;
+    p->path = dims == 2 && fused_supported(W, H, m1, m2, &Rf, &Ri) ? 1 : 0;
     p->R = p->path == 1 ? Rf : H;
     p->P = H / p->R;
     p->Ri = p->path == 1 ? Ri : H;
@@ -250,12 +291,16 @@ fno_plan_s* plan_new(int B, int Cin, int Cout, int H, int W, int m1, int m2,
     p->off_X = off; off = align_up(off + X_bytes(p), 256);
     p->off_Z = off; off = align_up(off + Z_bytes(p), 256);
     p->off_T = off;
-    if (p->path == 0) {
+    if (p->path == 0 && dims == 2) {
         const size_t planes = (size_t)B * (Cin > Cout ? Cin : Cout);
         off = align_up(off + 8ull * planes * H * m2, 256);
     }
     p->ws_bytes = off;
-    if (p->path == 1) {
+    if (dims == 1) {
+        describe_1d(p);
+        std::snprintf(p->desc, sizeof(p->desc), "1d-dft: rows(L=%d,m=%d)|%s|irows", W, m2,
+                      mix_name(p));
+    } else if (p->path == 1) {
         describe_fused(p);
         std::snprintf(p->desc, sizeof(p->desc),
                       "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|%s|inv-cols+rows(R=%d,P=%d)", W,
@@ -393,7 +438,7 @@ fno_status_t fno_plan_backward(fno_plan_t p, const float* x, const void* w, cons
     if (e == cudaSuccess && gx) e = run_inverse(q, A, gx, T, s, nullptr);
     if (e == cudaSuccess && gw) e = run_forward(*p, x, A, T, s, nullptr);
     if (e == cudaSuccess && gw)
-        e = p->nm >= 32 ? launch_wgrad_wide(*p, A, G, static_cast<float2*>(gw), s)
+        e = wgrad_wide_supported(p->nm) ? launch_wgrad_wide(*p, A, G, static_cast<float2*>(gw), s)
                         : launch_wgrad(A, G, static_cast<float2*>(gw), p->B, p->Cin, p->Cout,
                                        p->nm, p->m2, p->W, s);
     return cuda_status(e);

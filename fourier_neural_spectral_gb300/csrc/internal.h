@@ -54,7 +54,8 @@ constexpr int kMaxKernels = 8;
 
 struct fno_plan_s {
     int B, Cin, Cout, H, W, m1, m2;
-    int nm;                 // retained modes per plane: 2*m1*m2
+    int dims;               // 2, or 1 for the 1D layer (H = 1, W = L, m1 = 0, m2 = m)
+    int nm;                 // retained modes per plane: 2*m1*m2 (m2 for the 1D layer)
     fno_precision_t prec;
     int device;
     float scale;            // 1/sqrt(H*W), rounded once from double
@@ -108,6 +109,7 @@ cudaError_t launch_mix_tma(const fno_plan_s& p, const float2* X, const float2* w
 // fp32 contraction over blocks of 32 consecutive modes (mix_wide.cu).
 cudaError_t mix_wide_init();
 bool mix_wide_supported(int B, int Cin, int Cout, int nm);
+bool wgrad_wide_supported(int nm);
 // after_own_forward: the kernel just before this one is the library's forward
 // stage (w may then be fetched before the programmatic-launch wait).
 cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
@@ -142,6 +144,10 @@ cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, f
                                cudaStream_t s, fno_launch_ctx* ctx);
 cudaError_t launch_inverse_dft(const fno_plan_s& p, const float2* Z, float* y, float2* T,
                                cudaStream_t s, fno_launch_ctx* ctx);
+cudaError_t launch_forward_1d(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s,
+                              fno_launch_ctx* ctx);
+cudaError_t launch_inverse_1d(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s,
+                              fno_launch_ctx* ctx);
 
 // Stage launchers (all asynchronous on stream s).
 // Each launcher calls ctx->mark(s) after every kernel it enqueues.

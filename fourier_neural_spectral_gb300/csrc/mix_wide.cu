@@ -333,6 +333,10 @@ cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* 
 
 // Weight gradient gw[i][o][m] = c(k2) * sum_b conj(X[b][i][m]) * G[b][o][m] for
 // the plan p (X [B][Cin][nm], G [B][Cout][nm], gw [Cin][Cout][nm]).
+// the weight gradient's tile is fixed (16 rows); the 256-byte TMA rows need an
+// even mode count (a 16-byte row pitch)
+bool wgrad_wide_supported(int nm) { return nm >= kModes && (nm & 1) == 0; }
+
 cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2* G, float2* gw,
                               cudaStream_t s) {
     using T = WideTile<16>;

@@ -31,7 +31,7 @@ __device__ __forceinline__ int kr(int r, int H, int m1) { return r < m1 ? r : H 
 // j + 8, ..., lanes striding over w, then a shuffle reduction.
 __global__ void __launch_bounds__(kDftThreads)
 dft_rows_fwd_kernel(const float* __restrict__ x, float2* __restrict__ T, long long nrows, int W,
-                    int m2, int RB, const float2* __restrict__ tw_w) {
+                    int m2, int RB, float out_scale, const float2* __restrict__ tw_w) {
     extern __shared__ float2 dsm[];
     float2* tw = dsm;                                  // [W]
     float* xs = reinterpret_cast<float*>(dsm + W);     // [RB][W]
@@ -60,7 +60,7 @@ dft_rows_fwd_kernel(const float* __restrict__ x, float2* __restrict__ T, long lo
             re += __shfl_xor_sync(0xffffffffu, re, o);
             im += __shfl_xor_sync(0xffffffffu, im, o);
         }
-        if (lane == 0) T[(row0 + r) * m2 + k2] = make_float2(re, im);
+        if (lane == 0) T[(row0 + r) * m2 + k2] = make_float2(re * out_scale, im * out_scale);
     }
 }
 
@@ -207,7 +207,7 @@ cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, f
     const int RB = rows_per_cta(p.W);
     const size_t smem = sizeof(float2) * p.W + sizeof(float) * (size_t)RB * p.W;
     dft_rows_fwd_kernel<<<(unsigned)((nrows + RB - 1) / RB), kDftThreads, smem, s>>>(
-        x, T, nrows, p.W, p.m2, RB, p.tw_w);
+        x, T, nrows, p.W, p.m2, RB, 1.f, p.tw_w);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     if (e != cudaSuccess) return e;
@@ -233,6 +233,32 @@ cudaError_t launch_inverse_dft(const fno_plan_s& p, const float2* Z, float* y, f
     dft_rows_inv_kernel<<<(unsigned)((nrows + RB - 1) / RB), kDftThreads, smem, s>>>(
         T, y, nrows, p.W, p.m2, RB, p.scale, p.tw_w);
     e = cudaGetLastError();
+    if (e == cudaSuccess && ctx) e = ctx->mark(s);
+    return e;
+}
+
+// The 1D layer (plan with dims = 1, W = L, m2 = m retained modes): the row
+// transforms alone, orthonormal scale 1/sqrt(L) applied on each side.
+cudaError_t launch_forward_1d(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s,
+                              fno_launch_ctx* ctx) {
+    const long long nrows = (long long)p.B * p.Cin;
+    const int RB = rows_per_cta(p.W);
+    const size_t smem = sizeof(float2) * p.W + sizeof(float) * (size_t)RB * p.W;
+    dft_rows_fwd_kernel<<<(unsigned)((nrows + RB - 1) / RB), kDftThreads, smem, s>>>(
+        x, X, nrows, p.W, p.m2, RB, p.scale, p.tw_w);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && ctx) e = ctx->mark(s);
+    return e;
+}
+
+cudaError_t launch_inverse_1d(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s,
+                              fno_launch_ctx* ctx) {
+    const long long nrows = (long long)p.B * p.Cout;
+    const int RB = rows_per_cta(p.W);
+    const size_t smem = sizeof(float2) * p.W + sizeof(float2) * (size_t)RB * p.m2;
+    dft_rows_inv_kernel<<<(unsigned)((nrows + RB - 1) / RB), kDftThreads, smem, s>>>(
+        Z, y, nrows, p.W, p.m2, RB, p.scale, p.tw_w);
+    cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }

@@ -38,7 +38,7 @@ EXPORTS = (
     "fno_plan_describe", "fno_plan_kernel_info", "fno_plan_record_events", "fno_plan_execute", "fno_plan_destroy", "fno_spectral_conv2d",
     "fno_release_cache", "fno_forward_modes", "fno_mix_modes", "fno_inverse_modes",
     "fno_get_device_status", "fno_spectral_conv2d_noalloc", "fno_plan_backward",
-    "fno_block_epilogue", "fno_block_execute",
+    "fno_block_epilogue", "fno_block_execute", "fno_plan_create_1d",
 )
 
 
@@ -68,6 +68,7 @@ def load_library(path: str = LIB_PATH):
         sig = {
             "fno_status_string": (ctypes.c_char_p, [st]),
             "fno_plan_create": (st, [ctypes.POINTER(vp), i, i, i, i, i, i, i, i]),
+            "fno_plan_create_1d": (st, [ctypes.POINTER(vp), i, i, i, i, i, i]),
             "fno_plan_workspace_size": (st, [vp, ctypes.POINTER(sz)]),
             "fno_plan_launch_count": (st, [vp, ctypes.POINTER(i)]),
             "fno_plan_describe": (st, [vp, ctypes.c_char_p, sz]),
@@ -136,17 +137,23 @@ def _weight_ptr(w) -> int:
     return _ptr(w)
 
 
+def _precision(precision) -> int:
+    return PRECISIONS[precision] if isinstance(precision, str) else int(precision)
+
+
 class Plan:
     """fno_plan_t owner.  Holds its workspace as a torch tensor on the device."""
 
     def __init__(self, B, Cin, Cout, H, W, m1, m2, precision="fp32", allocate_workspace=True):
-        lib = load_library()
-        prec = PRECISIONS[precision] if isinstance(precision, str) else int(precision)
         h = ctypes.c_void_p()
-        _check(lib.fno_plan_create(ctypes.byref(h), B, Cin, Cout, H, W, m1, m2, prec),
-               "fno_plan_create")
+        _check(load_library().fno_plan_create(ctypes.byref(h), B, Cin, Cout, H, W, m1, m2,
+                                              _precision(precision)), "fno_plan_create")
+        self._setup(h, (B, Cin, Cout, H, W, m1, m2), precision, allocate_workspace)
+
+    def _setup(self, h, shape, precision, allocate_workspace):
+        lib = load_library()
         self._h = h
-        self.shape = (B, Cin, Cout, H, W, m1, m2)
+        self.shape = shape
         self.precision = precision
         n = ctypes.c_size_t()
         _check(lib.fno_plan_workspace_size(h, ctypes.byref(n)), "fno_plan_workspace_size")
@@ -257,6 +264,18 @@ class Plan:
             pass
 
 
+class Plan1d(Plan):
+    """fno_plan_create_1d owner: the 1D layer over x float32 [B, Cin, L] with
+    w complex64 [Cin, Cout, m] and y float32 [B, Cout, L]; every Plan method
+    applies (execute, stages, backward, block epilogue)."""
+
+    def __init__(self, B, Cin, Cout, L, m, precision="fp32", allocate_workspace=True):
+        h = ctypes.c_void_p()
+        _check(load_library().fno_plan_create_1d(ctypes.byref(h), B, Cin, Cout, L, m,
+                                                 _precision(precision)), "fno_plan_create_1d")
+        self._setup(h, (B, Cin, Cout, L, m), precision, allocate_workspace)
+
+
 def fno_spectral_conv2d(x, w, y, B, Cin, Cout, H, W, m1, m2, stream=None):
     """One-shot call with the exact C signature (fp32 path, cached plan)."""
     _check(load_library().fno_spectral_conv2d(_ptr(x), _weight_ptr(w), _ptr(y), B, Cin, Cout, H,
@@ -295,6 +314,16 @@ def _autograd_plan(B, Cin, Cout, H, W, m1, m2, device):
     return plan
 
 
+def _autograd_plan_1d(B, Cin, Cout, L, m, device):
+    key = ("1d", B, Cin, Cout, L, m, device)
+    plan = _autograd_plans.get(key)
+    if plan is None:
+        with torch.cuda.device(device):
+            plan = Plan1d(B, Cin, Cout, L, m)
+        _autograd_plans[key] = plan
+    return plan
+
+
 class SpectralConv2dFunction(torch.autograd.Function):
     """y = layer(x, w) with gradients for x (float32 [B, Cin, H, W]) and w
     (complex64 [Cin, Cout, 2*m1, m2]) through fno_plan_execute and
@@ -327,6 +356,39 @@ class SpectralConv2dFunction(torch.autograd.Function):
 def spectral_conv2d_autograd(x: torch.Tensor, w: torch.Tensor, m1: int, m2: int):
     """Differentiable layer (see SpectralConv2dFunction)."""
     return SpectralConv2dFunction.apply(x, w, m1, m2)
+
+
+class SpectralConv1dFunction(torch.autograd.Function):
+    """The 1D layer with gradients for x (float32 [B, Cin, L]) and w
+    (complex64 [Cin, Cout, m]); plans cached per (shape, device) as for
+    SpectralConv2dFunction."""
+
+    @staticmethod
+    def forward(ctx, x, w, m):
+        B, Cin, L = x.shape
+        Cout = w.shape[1]
+        plan = _autograd_plan_1d(B, Cin, Cout, L, m, x.device.index)
+        y = torch.empty((B, Cout, L), dtype=torch.float32, device=x.device)
+        plan.fno_plan_execute(x, w, y)
+        ctx.save_for_backward(x, w)
+        ctx.plan = plan
+        return y
+
+    @staticmethod
+    def backward(ctx, gy):
+        x, w = ctx.saved_tensors
+        gy = gy.contiguous()
+        gx = torch.empty_like(x) if ctx.needs_input_grad[0] else None
+        gw = torch.empty_like(w) if ctx.needs_input_grad[1] else None
+        if gx is None and gw is None:
+            return None, None, None
+        ctx.plan.fno_plan_backward(x, w, gy, gx, gw)
+        return gx, gw, None
+
+
+def spectral_conv1d_autograd(x: torch.Tensor, w: torch.Tensor, m: int):
+    """Differentiable 1D layer (see SpectralConv1dFunction)."""
+    return SpectralConv1dFunction.apply(x, w, m)
 
 
 def fno_release_cache():

@@ -84,6 +84,21 @@ const char* fno_status_string(fno_status_t status);
 fno_status_t fno_plan_create(fno_plan_t* plan, int B, int Cin, int Cout, int H, int W,
                              int m1, int m2, fno_precision_t prec);
 
+/* Create a plan for the 1D layer over sequences of L points on the CURRENT
+ * device: y = irfft(Z, n=L, norm="ortho") with X = rfft(x, norm="ortho") and
+ * Z[b,o,k] = sum_i X[b,i,k] w[i,o,k] for the m retained modes k < m (the
+ * others zero; C2R drops the imaginary part of the k = 0 and k = L/2 bins).
+ * Sources: FFT operator-optimisation page, section 3.2 (the transform over a
+ * sequence, a learned complex factor per frequency, the inverse back), with the
+ * per-mode channel contraction of the TurboFNO page, section 2.2, in one
+ * dimension.  Shapes: x float [B][Cin][L], w complex64 [Cin][Cout][m],
+ * y float [B][Cout][L]; 2 <= L <= 4096, 1 <= m <= L/2 + 1 (any L: direct
+ * DFTs).  The returned plan serves every call taking a plan (execute, the
+ * three stages, the backward, the block epilogue), with H = 1, W = L, and
+ * 2*m1*m2 read as m wherever a size is stated.  Errors as fno_plan_create. */
+fno_status_t fno_plan_create_1d(fno_plan_t* plan, int B, int Cin, int Cout, int L, int m,
+                                fno_precision_t prec);
+
 /* Bytes of device workspace fno_plan_execute needs (may be 0). */
 fno_status_t fno_plan_workspace_size(fno_plan_t plan, size_t* bytes);
 

@@ -304,6 +304,18 @@ def block(x, w, w_pw, bias, m1: int, m2: int, activation: str = "gelu") -> np.nd
     return y
 
 
+def block1d(x, w, w_pw, bias, m: int, activation: str = "gelu") -> np.ndarray:
+    """The block around the 1D layer: act(spectral_conv1d(x, w) + w_pw x + bias),
+    x [B, Cin, L]; the pointwise branch is the 2D one over a 1 x L grid."""
+    x = _real(x)
+    B, Cin, L = x.shape
+    y = spectral_conv1d(x, w, m) + pointwise(x.reshape(B, Cin, 1, L), w_pw, bias)[:, :, 0, :]
+    if activation == "gelu":
+        return gelu(y)
+    assert activation == "none"
+    return y
+
+
 def forward_modes_parallel(x, m1: int, m2: int, threads: int | None = None) -> np.ndarray:
     """forward_modes over independent planes on several host threads.
 

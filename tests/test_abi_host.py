@@ -59,6 +59,22 @@ def test_plan_create_rejects_bad_shapes(lib, shape, code):
     assert not h.value
 
 
+@pytest.mark.parametrize("shape,code", [
+    ((0, 4, 4, 64, 8), 1),       # B = 0
+    ((2, 0, 4, 64, 8), 1),       # Cin = 0
+    ((2, 4, 4, 64, 0), 1),       # no modes
+    ((2, 4, 4, 64, 34), 1),      # m > L/2 + 1
+    ((2, 4, 4, 15, 9), 1),       # m > L/2 + 1 for odd L
+    ((2, 4, 4, 1, 1), 2),        # L = 1
+    ((2, 4, 4, 8192, 8), 2),     # L above 4096
+])
+def test_plan_create_1d_rejects_bad_shapes(lib, shape, code):
+    h = ctypes.c_void_p(1234)
+    rc = lib.fno_plan_create_1d(ctypes.byref(h), *shape, 0)
+    assert rc == code
+    assert not h.value
+
+
 def test_plan_create_rejects_bad_precision(lib):
     h = ctypes.c_void_p()
     assert lib.fno_plan_create(ctypes.byref(h), 2, 4, 4, 16, 16, 4, 4, 7) == 1

@@ -7,6 +7,8 @@ computes exactly the orthonormal irfft2(Z, s=(H, W)) of the layer's
 definition.  Together they fail on a dropped term, a wrong sign or index, a
 transposed operand, a wrong scale or a wrong retained-row order.
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -458,3 +460,22 @@ def test_backward_1d_identities(L, m):
     assert abs(lhs - np.sum(x * gx)) <= 1e-12 * np.abs(x * gx).sum()
     lhs = np.sum(oracle.spectral_conv1d(x, v, m) * g)
     assert abs(lhs - np.real(np.sum(np.conj(gw) * v))) <= 1e-12 * np.abs(np.conj(gw) * v).sum()
+
+
+def test_block_1d_special_cases():
+    B, Cin, Cout, L, m = 2, 3, 2, 12, 5
+    x = RNG.standard_normal((B, Cin, L))
+    w = RNG.standard_normal((Cin, Cout, m)) + 1j * RNG.standard_normal((Cin, Cout, m))
+    # no pointwise branch, bias or activation: the 1D layer itself
+    assert np.allclose(oracle.block1d(x, w, np.zeros((Cout, Cin)), np.zeros(Cout), m, "none"),
+                       oracle.spectral_conv1d(x, w, m), rtol=1e-13, atol=1e-13)
+    # no spectral weights: each output point is GELU(bias + sum_i w_pw x), by hand
+    wpw = RNG.standard_normal((Cout, Cin))
+    bias = RNG.standard_normal(Cout)
+    out = oracle.block1d(x, np.zeros_like(w), wpw, bias, m)
+    for b in range(B):
+        for o in range(Cout):
+            for n in range(L):
+                v = bias[o] + sum(wpw[o, i] * x[b, i, n] for i in range(Cin))
+                want = 0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0)))
+                assert abs(out[b, o, n] - want) < 1e-12
