@@ -93,6 +93,32 @@ __device__ __forceinline__ void dft(float2 (&v)[N]) {
     Dft<N, SGN>::run(v);
 }
 
+// The 16-point DFT of a sequence whose only nonzero entries are e[0..3] and
+// e[12..15] (indices m = -4..3 mod 16), e[4..11] being ignored.  Splitting the
+// outputs by parity,
+//   X[2k]     = sum_m e_m w8^{mk},              w8 = e^{SGN 2 pi i / 8},
+//   X[2k + 1] = sum_m (e_m w16^m) w8^{mk},       w16 = e^{SGN 2 pi i / 16},
+// i.e. two 8-point DFTs over m mod 8, which skips the additions of the zero
+// entries that a full 16-point transform would perform.
+template <int SGN>
+__device__ __forceinline__ void dft16_in8(float2 (&e)[16]) {
+    float2 a[8], b[8];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        a[r] = e[r];
+        a[4 + r] = e[12 + r];
+        b[r] = rot16<SGN>(e[r], r);
+        b[4 + r] = rot16<SGN>(e[12 + r], 12 + r);
+    }
+    dft<8, SGN>(a);
+    dft<8, SGN>(b);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        e[2 * k] = a[k];
+        e[2 * k + 1] = b[k];
+    }
+}
+
 // e^{SGN * 2 pi i * j / N} from a table tab[j] = e^{+2 pi i j / N}, j reduced mod N.
 template <int SGN>
 __device__ __forceinline__ float2 root(const float2* __restrict__ tab, int j, int N) {

@@ -27,27 +27,34 @@ namespace fno {
 namespace {
 
 constexpr int kModes = 32;  // modes per CTA (one per lane)
-constexpr int kOCB = 8;     // output channels per CTA
-constexpr int kJO = 4;      // output channels per thread (two warp halves)
-constexpr int kNST = 2;     // ring depth
-// Stage size and ring depth, measured (128x128 / 256x256 / 2048x2048 contraction, us):
-// 4 x 12 KB 37.6 / 206 / 19.9, 3 x 18 KB 36.1 / 208 / 18.6, 2 x 24 KB 35.3 / 197 / 18.8,
-// 6 x 8 KB 45.8 / 201 / 20.7: fewer, larger stages win.
-constexpr size_t kStageTarget = 24 * 1024;
 constexpr size_t kRowBytes = kModes * sizeof(float2);  // 256
 
-// Per batch tile BT (a power of two <= 16): batch rows per thread, consumer
-// warps along the batch, and input channels per stage.
+// Per batch tile BT (a power of two <= 16): output channels per CTA (OCB) and
+// per thread (JO), batch rows per thread (JB), consumer warps (OCB/JO along the
+// outputs x BT/JB along the batch), ring depth and input channels per stage.
+// Stage size and ring depth, measured (128x128 / 256x256 / 2048x2048
+// contraction, us): 4 x 12 KB 37.6 / 206 / 19.9, 3 x 18 KB 36.1 / 208 / 18.6,
+// 2 x 24 KB 35.3 / 197 / 18.8, 6 x 8 KB 45.8 / 201 / 20.7.  An 8 x 8 thread tile
+// over 16 outputs per CTA (two CTAs per SM, half the X re-reads) measured the
+// same at 128x128 (35.4 against 35.0 us), as did 8 x 4 tiles and the
+// three-multiplication complex product: the FMA stream of this loop is the
+// bound, not its loads.
 template <int BT>
 struct WideTile {
+    static constexpr int OCB = 8;
+    static constexpr int JO = 4;
     static constexpr int JB = BT >= 2 ? BT / 2 : 1;
-    static constexpr int NBW = BT / JB;
-    static constexpr int IC = (int)(kStageTarget / (kRowBytes * (kOCB + BT)));
-    static constexpr int Consumers = 2 * NBW;  // warps
+    static constexpr int NOW = OCB / JO;  // consumer warps along the outputs
+    static constexpr int NBW = BT / JB;   // consumer warps along the batch
+    static constexpr int NST = 2;
+    static constexpr int MinBlocks = 4;
+    static constexpr size_t StageTarget = 24 * 1024;
+    static constexpr int IC = (int)(StageTarget / (kRowBytes * (OCB + BT)));
+    static constexpr int Consumers = NOW * NBW;  // warps
     static constexpr int Threads = 32 * (Consumers + 1);  // + one producer warp
-    static constexpr uint32_t WBytes = (uint32_t)(kRowBytes * kOCB * IC);
-    static constexpr uint32_t StageBytes = (uint32_t)(kRowBytes * IC * (kOCB + BT));
-    static constexpr size_t Smem = 128 + (size_t)kNST * StageBytes;
+    static constexpr uint32_t WBytes = (uint32_t)(kRowBytes * OCB * IC);
+    static constexpr uint32_t StageBytes = (uint32_t)(kRowBytes * IC * (OCB + BT));
+    static constexpr size_t Smem = 128 + (size_t)NST * StageBytes;
 };
 
 int wide_bt(int B) {
@@ -89,12 +96,12 @@ size_t wide_smem(int bt) {
 enum { kMix = 0, kAdj = 1, kWgrad = 2 };
 
 template <int BT, int MODE>
-__global__ void __launch_bounds__(WideTile<BT>::Threads, 4)
+__global__ void __launch_bounds__(WideTile<BT>::Threads, WideTile<BT>::MinBlocks)
 mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 float2* __restrict__ Z, int rows, int red, int Cout, int NM, int m2, int W,
                 int early_w, unsigned* __restrict__ err) {
     using T = WideTile<BT>;
-    constexpr int JB = T::JB, IC = T::IC;
+    constexpr int JB = T::JB, IC = T::IC, kOCB = T::OCB, kJO = T::JO, kNST = T::NST;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kNST;
@@ -173,7 +180,7 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     // ---- consumers ------------------------------------------------------
     griddep_wait();  // Z may still be read by an earlier kernel until then
     griddep_launch_dependents();
-    const int oh = warp & 1, bh = warp >> 1;
+    const int oh = warp % T::NOW, bh = warp / T::NOW;
     float2 acc[kJO][JB];
 #pragma unroll
     for (int j = 0; j < kJO; ++j)
@@ -253,6 +260,7 @@ cudaError_t set_attr() {
 template <int BT>
 cudaError_t launch_bt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, const fno_plan_s& p,
                       int early_w, cudaStream_t s) {
+    constexpr int kOCB = WideTile<BT>::OCB;
     const dim3 grid(((p.nm + kModes - 1) / kModes) * ((p.Cout + kOCB - 1) / kOCB), 1,
                     (p.B + BT - 1) / BT);
     if (p.adjoint)
@@ -304,16 +312,16 @@ cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* 
                             bool after_own_forward, cudaStream_t s, fno_launch_ctx* ctx) {
     const int early_w = after_own_forward ? 1 : 0;
     const int bt = wide_bt(p.B);
-    int ic = 0;
+    int ic = 0, kOCB = 0;
     switch (bt) {
-        case 1: ic = WideTile<1>::IC; break;
-        case 2: ic = WideTile<2>::IC; break;
-        case 4: ic = WideTile<4>::IC; break;
-        case 8: ic = WideTile<8>::IC; break;
-        default: ic = WideTile<16>::IC; break;
+        case 1: ic = WideTile<1>::IC; kOCB = WideTile<1>::OCB; break;
+        case 2: ic = WideTile<2>::IC; kOCB = WideTile<2>::OCB; break;
+        case 4: ic = WideTile<4>::IC; kOCB = WideTile<4>::OCB; break;
+        case 8: ic = WideTile<8>::IC; kOCB = WideTile<8>::OCB; break;
+        default: ic = WideTile<16>::IC; kOCB = WideTile<16>::OCB; break;
     }
     // w is [Cin_w][Cout_w][NM]: for an adjoint plan Cin_w = p.Cout (its outputs)
-    // and Cout_w = p.Cin (its reduction), boxes (32 modes, IC, 8)
+    // and Cout_w = p.Cin (its reduction), boxes (32 modes, IC, OCB)
     CUtensorMap mw, mx;
     const bool ok_w = p.adjoint ? encode_wide_map(&mw, w, p.nm, p.Cin, p.Cout, ic, kOCB)
                                 : encode_wide_map(&mw, w, p.nm, p.Cout, p.Cin, kOCB, ic);
@@ -331,15 +339,16 @@ cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* 
     return e;
 }
 
-// Weight gradient gw[i][o][m] = c(k2) * sum_b conj(X[b][i][m]) * G[b][o][m] for
-// the plan p (X [B][Cin][nm], G [B][Cout][nm], gw [Cin][Cout][nm]).
-// the weight gradient's tile is fixed (16 rows); the 256-byte TMA rows need an
-// even mode count (a 16-byte row pitch)
+// The weight gradient's tile is fixed (16 rows); the 256-byte TMA rows need an
+// even mode count (a 16-byte row pitch).
 bool wgrad_wide_supported(int nm) { return nm >= kModes && (nm & 1) == 0; }
 
+// Weight gradient gw[i][o][m] = c(k2) * sum_b conj(X[b][i][m]) * G[b][o][m] for
+// the plan p (X [B][Cin][nm], G [B][Cout][nm], gw [Cin][Cout][nm]).
 cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2* G, float2* gw,
                               cudaStream_t s) {
     using T = WideTile<16>;
+    constexpr int kOCB = T::OCB;
     CUtensorMap mg, mx;
     if (!encode_wide_map(&mg, G, p.nm, p.Cout, p.B, kOCB, T::IC) ||
         !encode_wide_map(&mx, X, p.nm, p.Cin, p.B, 16, T::IC))

@@ -284,9 +284,11 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
 
     const int g = threadIdx.x / L, t = threadIdx.x % L;
     const int kk2 = t / G, a = t % G;
+    // second-pass twiddles times the output scale 1/sqrt(HW) (the transform is
+    // linear, so scaling its inputs scales the rows it writes)
     float2 tw1[16], tw2[NK];
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) tw1[kk] = root<1>(tw_w, t * kk, W);
+    for (int kk = 0; kk < 16; ++kk) tw1[kk] = cscale(root<1>(tw_w, t * kk, W), scale);
 #pragma unroll
     for (int j = 0; j < NK; ++j) tw2[j] = root<1>(tw_w, 16 * a * cand_k1<L>(j), W);
     float2* S = scr + g * B::GroupScr;  // S[kk][n1], row stride L + G
@@ -316,7 +318,9 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
                 const float2 u = k <= half ? uk : um;
                 e[k1 & 15] = cmul(u, tw2[j]);
             }
-            dft<16, 1>(e);
+            // the candidates k1 = 0..3 and L-4..L-1 fill e[0..3] and e[12..15] only
+            static_assert(L % 16 == 0 && 2 * kNL == 8, "candidate residues 0..3, 12..15");
+            dft16_in8<1>(e);
 #pragma unroll
             for (int b = 0; b < 16; ++b) S[kk2 * B::SStride + a + G * b] = e[b];
         }
@@ -325,14 +329,14 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
             float2 v[16];
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk)
-                v[kk] = kk == 0 ? S[t] : cmul(S[kk * B::SStride + t], tw1[kk]);
+                v[kk] = kk == 0 ? cscale(S[t], scale) : cmul(S[kk * B::SStride + t], tw1[kk]);
             dft<16, 1>(v);
             float* ya = yp + (size_t)(p + P * qa) * W;
             float* yb = ya + (size_t)P * W;
 #pragma unroll
             for (int n2 = 0; n2 < 16; ++n2) {
-                ya[t + L * n2] = v[n2].x * scale;
-                yb[t + L * n2] = v[n2].y * scale;
+                ya[t + L * n2] = v[n2].x;
+                yb[t + L * n2] = v[n2].y;
             }
         }
         group_sync<L>(g);

@@ -202,13 +202,16 @@ __device__ __forceinline__ void row_pair_forward(const float* __restrict__ ra,
 // The thread's first-pass twiddles e^{+2 pi i n1 kk / W} for its bins kk,
 // loaded once per kernel: twi[(ps * 2 + side) * Bq + n1] with side 0 for bin
 // pair_a(p), 1 for pair_b(p) (and twi[n1] = e^{+2 pi i n1 t / W} when Bq = 16).
+// The twiddles carry the output scale 1/sqrt(HW) (the row transform is linear,
+// so scaling the first pass's outputs scales the rows); the n1 = 0 terms, which
+// take no twiddle, are scaled where they are stored.
 template <int W>
 __device__ __forceinline__ void inverse_twiddles(float2 (&twi)[16], int t,
-                                                 const float2* __restrict__ tw) {
+                                                 const float2* __restrict__ tw, float scale) {
     constexpr int Bq = W / 16;
     if constexpr (Bq == 16) {
 #pragma unroll
-        for (int n1 = 0; n1 < 16; ++n1) twi[n1] = root<1>(tw, n1 * t, W);
+        for (int n1 = 0; n1 < 16; ++n1) twi[n1] = cscale(root<1>(tw, n1 * t, W), scale);
     } else {
         constexpr int NP = 8 / Bq;
 #pragma unroll
@@ -216,8 +219,8 @@ __device__ __forceinline__ void inverse_twiddles(float2 (&twi)[16], int t,
             const int p = t + Bq * ps;
 #pragma unroll
             for (int n1 = 0; n1 < Bq; ++n1) {
-                twi[(ps * 2) * Bq + n1] = root<1>(tw, n1 * pair_a(p), W);
-                twi[(ps * 2 + 1) * Bq + n1] = root<1>(tw, n1 * pair_b(p), W);
+                twi[(ps * 2) * Bq + n1] = cscale(root<1>(tw, n1 * pair_a(p), W), scale);
+                twi[(ps * 2 + 1) * Bq + n1] = cscale(root<1>(tw, n1 * pair_b(p), W), scale);
             }
         }
     }
@@ -252,7 +255,7 @@ __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2*
             dft<16, 1>(u);
 #pragma unroll
             for (int n1 = 0; n1 < 16; ++n1)
-                S[n1 * RS + kk] = n1 == 0 ? u[0] : cmul(u[n1], twi[n1]);
+                S[n1 * RS + kk] = n1 == 0 ? cscale(u[0], scale) : cmul(u[n1], twi[n1]);
         } else {
             constexpr int NP = 8 / Bq;
 #pragma unroll
@@ -290,8 +293,10 @@ __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2*
                 dft<Bq, 1>(ub);
 #pragma unroll
                 for (int n1 = 0; n1 < Bq; ++n1) {
-                    S[n1 * RS + ka] = n1 == 0 ? ua[0] : cmul(ua[n1], twi[(ps * 2) * Bq + n1]);
-                    S[n1 * RS + kb] = n1 == 0 ? ub[0] : cmul(ub[n1], twi[(ps * 2 + 1) * Bq + n1]);
+                    S[n1 * RS + ka] =
+                        n1 == 0 ? cscale(ua[0], scale) : cmul(ua[n1], twi[(ps * 2) * Bq + n1]);
+                    S[n1 * RS + kb] =
+                        n1 == 0 ? cscale(ub[0], scale) : cmul(ub[n1], twi[(ps * 2 + 1) * Bq + n1]);
                 }
             }
         }
@@ -304,8 +309,8 @@ __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2*
         dft<16, 1>(v);
 #pragma unroll
         for (int n2 = 0; n2 < 16; ++n2) {
-            ya[t + Bq * n2] = v[n2].x * scale;
-            yb[t + Bq * n2] = v[n2].y * scale;
+            ya[t + Bq * n2] = v[n2].x;
+            yb[t + Bq * n2] = v[n2].y;
         }
     }
     __syncwarp();
@@ -418,7 +423,7 @@ inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int
         const int g = threadIdx.x / Bq, t = threadIdx.x % Bq;
         float2* S = scr + g * C::RowScr;
         float2 twi[16];
-        inverse_twiddles<W>(twi, t, tw_w);
+        inverse_twiddles<W>(twi, t, tw_w, scale);
         float* yp = y + (size_t)plane * H * W;
         constexpr int npairs = R / 2;
         constexpr int iters = (npairs + C::RowGroups - 1) / C::RowGroups;
