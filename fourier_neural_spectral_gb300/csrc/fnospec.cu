@@ -330,10 +330,11 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
     std::vector<float2> th = twiddles(H), tw = twiddles(W);
     cudaError_t e = cudaMalloc(&p->tw_h, sizeof(float2) * H);
     if (e == cudaSuccess) e = cudaMalloc(&p->tw_w, sizeof(float2) * W);
-    if (e == cudaSuccess) e = cudaMalloc(&p->err, sizeof(unsigned));
+    // err[0]: error bits, err[1]: debug flags (see fno_plan_debug_force_timeout)
+    if (e == cudaSuccess) e = cudaMalloc(&p->err, 2 * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemcpy(p->tw_h, th.data(), sizeof(float2) * H, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(p->tw_w, tw.data(), sizeof(float2) * W, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMemset(p->err, 0, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemset(p->err, 0, 2 * sizeof(unsigned));
     if (e != cudaSuccess) {
         fno_plan_destroy(p);
         return nullptr;
@@ -557,6 +558,17 @@ fno_status_t fno_inverse_modes(fno_plan_t p, const void* Z, float* y, void* ws, 
         return FNO_ERR_INVALID_ARG;
     float2* T = reinterpret_cast<float2*>(static_cast<char*>(ws) + p->off_T);
     return cuda_status(run_inverse(*p, static_cast<const float2*>(Z), y, T, s, nullptr));
+}
+
+fno_status_t fno_plan_debug_force_timeout(fno_plan_t p, int enable) {
+    if (!p) return FNO_ERR_INVALID_ARG;
+    fno_status_t st = check_device(p);
+    if (st != FNO_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FNO_ERR_CUDA;
+    const unsigned flags = enable ? 1u : 0u;
+    if (cudaMemcpy(p->err + 1, &flags, sizeof(flags), cudaMemcpyHostToDevice) != cudaSuccess)
+        return FNO_ERR_CUDA;
+    return FNO_OK;
 }
 
 fno_status_t fno_get_device_status(fno_plan_t p, cudaStream_t s) {

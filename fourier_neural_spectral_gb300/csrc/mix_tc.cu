@@ -154,6 +154,7 @@ mix_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
     if (warp == 0) {
         // ---- TMA producer ----
         if (lane == 0) {
+            int issued = 0;
             for (int c = 0; c < nch; ++c) {
                 const int s = c % kNST;
                 if (c >= kNST &&
@@ -166,7 +167,14 @@ mix_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 mbar_arrive_expect_tx(&full[s], tx);
                 tma_load_3d(st, &tmW, 2 * m0, o0, c * kIC, &full[s]);
                 tma_load_3d(st + x_off, &tmX, 2 * m0, c * kIC, 0, &full[s]);
+                issued = c + 1;
             }
+            // No copy may be in flight when the ring is reused or the CTA leaves.
+            // Chunk c was refilled only after the converters had waited for
+            // chunk c - kNST, so only the last kNST issued chunks may still be
+            // landing (bounded waits that no error flag cuts short).
+            for (int c = issued > kNST ? issued - kNST : 0; c < issued; ++c)
+                wait_parity_bounded(&full[c % kNST], (uint32_t)((c / kNST) & 1), nullptr);
         }
     } else if (warp == 1) {
         // ---- MMA issuer ----
@@ -269,9 +277,14 @@ mix_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
     }
 
     // ---- epilogue: wait for the last MMA, then TMEM -> Z ----
+    // every issued MMA must complete before TMEM is read or released: this wait
+    // is not cut short by a forced timeout (the issuer always commits `done`)
     bool ok = true;
-    if (warp >= 2) ok = wait_parity_bounded(done, 0, err);
-    if (!ok) atomicExch(fail, 1);
+    if (warp >= 2) ok = wait_parity_bounded(done, 0, nullptr);
+    if (!ok) {
+        atomicExch(fail, 1);
+        atomicOr(err, 2u /* FNO_DEVERR_TIMEOUT */);
+    }
     __syncthreads();
     const bool good = *(volatile int*)fail == 0;
     tc_fence_after_sync();
@@ -314,13 +327,6 @@ mix_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ C
                 }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
-        }
-    }
-    if (!good && tid == 0) {
-        // drain TMA copies that may still be in flight into the ring
-        for (int s = 0; s < kNST && s < nch; ++s) {
-            const int last = ((nch - 1 - s) / kNST) * kNST + s;  // last chunk using stage s
-            wait_parity_bounded(&full[s], (uint32_t)((last / kNST) & 1), err);
         }
     }
     tc_fence_before_sync();

@@ -154,7 +154,7 @@ mix_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         // drain: wait (bounded) for every copy still in flight, then leave
         if (tid == 0)
             for (int c = consumed; c < issued; ++c)
-                wait_parity_bounded(&bars[c % kStages], (uint32_t)((c / kStages) & 1), err);
+                wait_parity_bounded(&bars[c % kStages], (uint32_t)((c / kStages) & 1), nullptr);
         __syncthreads();
         return;
     }

@@ -45,7 +45,7 @@ bool reachable(const void* p) {
 }
 
 // Fills both twiddle tables e^{+2 pi i j / N} (double sincospi, rounded once
-// to float) and clears the error word.  Nothing else in the scratch needs to
+// to float) and clears the error word and the debug-flag word after it.  Nothing else in the scratch needs to
 // start at zero: X, Z and T are fully written before they are read.
 __global__ void noalloc_setup_kernel(float2* tw_h, int H, float2* tw_w, int W, unsigned* err) {
     const int n = H + W;
@@ -60,7 +60,10 @@ __global__ void noalloc_setup_kernel(float2* tw_h, int H, float2* tw_w, int W, u
             tw_w[k] = make_float2((float)c, (float)s);
         }
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0u;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        err[0] = 0u;  // error bits
+        err[1] = 0u;  // debug flags (none)
+    }
 }
 
 }  // namespace
@@ -86,7 +89,7 @@ extern "C" fno_status_t fno_spectral_conv2d_noalloc(const float* x, const void* 
     size_t off = 0;
     const size_t off_th = off; off = align256(off + 8ull * H);
     const size_t off_tw = off; off = align256(off + 8ull * W);
-    const size_t off_err = off; off = align256(off + sizeof(unsigned));
+    const size_t off_err = off; off = align256(off + 2 * sizeof(unsigned));
     const size_t off_X = off; off = align256(off + 8ull * B * Cin * nm);
     const size_t off_Z = off; off = align256(off + 8ull * B * Cout * nm);
     const size_t off_T = off; off = align256(off + 8ull * planes * H * m2);

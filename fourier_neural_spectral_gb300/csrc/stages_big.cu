@@ -271,11 +271,12 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
     }
 
     if constexpr (ZS) {
-        if (!wait_parity_bounded(zbar, 0, err)) {
-            // err is set and the output is void; still wait (bounded) for the
-            // copy before the shared memory is rewritten
-            if (threadIdx.x == 0) wait_parity_bounded(zbar, 0, nullptr);
-        }
+        const bool zok = wait_parity_bounded(zbar, 0, err);
+        // on a timeout err is set and the output is void; thread 0 still waits
+        // (bounded) for the copy, and every thread for thread 0, before the
+        // shared memory is rewritten
+        if (!zok && threadIdx.x == 0) wait_parity_bounded(zbar, 0, nullptr);
+        __syncthreads();
         columns_inverse<R, 0, true>(scr, V, ys, sm, H, m1, m2, P, p, tw_h);
     } else {
         columns_inverse<R>(scr, V, ys, Zp, H, m1, m2, P, p, tw_h);

@@ -2,7 +2,7 @@
 // memory barriers (sm_90+ PTX ISA: mbarrier.*, cp.async.bulk.tensor.*), plus the
 // host-side lookup of cuTensorMapEncodeTiled through the runtime.
 //
-// Every wait is bounded: wait_parity_bounded polls for at most kWaitLimitNs of
+// Every wait is bounded: wait_parity_bounded waits for at most kWaitLimitNs of
 // %globaltimer time; on expiry it sets FNO_DEVERR_TIMEOUT in the error word and
 // returns false so the kernel can leave without hanging the GPU.
 #pragma once
@@ -61,13 +61,44 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns` while
+// the phase is incomplete; it resumes as soon as the phase completes.  A
+// suspended warp takes no issue slots, where a polling loop would spend them
+// on the timer reads, compares and branches of every retry.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+constexpr uint32_t kSleepHintNs = 100000;  // per retry; the total stays bounded below
+
 // Wait for phase `parity` of the barrier to complete, for at most kWaitLimitNs.
+// `err` points at the plan's two device words: err[0] collects error bits,
+// err[1] holds debug flags.  With bit 0 of err[1] set (the forced-timeout test
+// hook) every such wait gives up at once, as if its time had run out.  The flag
+// is written by the host between launches only, so the read-only cache may hold
+// it (one L2 read per SM, L1 hits after).  Waits that drain copies or MMAs still
+// in flight pass err = nullptr: they are bounded but never cut short, so that
+// no kernel leaves while an asynchronous operation can still write its shared
+// or tensor memory.
 __device__ __forceinline__ bool wait_parity_bounded(uint64_t* bar, uint32_t parity,
                                                     unsigned* err) {
+    if (err && (__ldg(err + 1) & 1u)) {
+        atomicOr(err, 2u /* FNO_DEVERR_TIMEOUT */);
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < kWaitLimitNs)
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (err) atomicOr(err, 2u /* FNO_DEVERR_TIMEOUT */);
     return false;
 }

@@ -39,6 +39,7 @@ EXPORTS = (
     "fno_release_cache", "fno_forward_modes", "fno_mix_modes", "fno_inverse_modes",
     "fno_get_device_status", "fno_spectral_conv2d_noalloc", "fno_plan_backward",
     "fno_block_epilogue", "fno_block_execute", "fno_plan_create_1d",
+    "fno_plan_debug_force_timeout",
 )
 
 
@@ -69,6 +70,7 @@ def load_library(path: str = LIB_PATH):
             "fno_status_string": (ctypes.c_char_p, [st]),
             "fno_plan_create": (st, [ctypes.POINTER(vp), i, i, i, i, i, i, i, i]),
             "fno_plan_create_1d": (st, [ctypes.POINTER(vp), i, i, i, i, i, i]),
+            "fno_plan_debug_force_timeout": (st, [vp, i]),
             "fno_plan_workspace_size": (st, [vp, ctypes.POINTER(sz)]),
             "fno_plan_launch_count": (st, [vp, ctypes.POINTER(i)]),
             "fno_plan_describe": (st, [vp, ctypes.c_char_p, sz]),
@@ -248,6 +250,12 @@ class Plan:
         arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
         self._event_array = arr  # keep alive while armed
         _check(lib.fno_plan_record_events(self._h, arr, len(events)), "fno_plan_record_events")
+
+    def fno_plan_debug_force_timeout(self, enable: bool):
+        """Test hook: make this plan's bounded device waits give up at once
+        (see include/fnospec.h)."""
+        _check(load_library().fno_plan_debug_force_timeout(self._h, 1 if enable else 0),
+               "fno_plan_debug_force_timeout")
 
     def fno_get_device_status(self, stream=None) -> int:
         return int(load_library().fno_get_device_status(self._h, _stream(stream)))

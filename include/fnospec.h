@@ -235,6 +235,21 @@ fno_status_t fno_spectral_conv2d_noalloc(const float* x, const void* w, float* y
  * FNO_OK, FNO_ERR_TIMEOUT or FNO_ERR_DEVICE (or FNO_ERR_CUDA if the copy fails). */
 fno_status_t fno_get_device_status(fno_plan_t plan, cudaStream_t s);
 
+/* Test hook for the failure path: with enable != 0, every bounded wait inside
+ * this plan's kernels (and its backward's) gives up at once, as if its time
+ * limit had run out.  The kernel sets
+ * FNO_DEVERR_TIMEOUT in the error word, lets its own asynchronous copies and
+ * tensor-core work finish, frees what it holds and returns, so the context
+ * stays usable; outputs of such calls are void and the next
+ * fno_get_device_status returns FNO_ERR_TIMEOUT.  Kernels without waits
+ * (the shape-generic and direct-DFT transforms, the short-row forward) are not
+ * affected.  enable = 0 restores normal operation.  Host-synchronous: it
+ * synchronises the device before it writes the flag, so call it between calls,
+ * never during stream capture.  Returns FNO_ERR_INVALID_ARG for a NULL plan or
+ * another current device, FNO_ERR_CUDA if the device copy fails.  A test hook
+ * of this library: no page defines it. */
+fno_status_t fno_plan_debug_force_timeout(fno_plan_t plan, int enable);
+
 #ifdef __cplusplus
 }
 #endif
