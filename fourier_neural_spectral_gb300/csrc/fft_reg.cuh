@@ -3,7 +3,8 @@
 //
 // dft<N, SGN>(v): v[k] <- sum_n v[n] * e^{SGN * 2 pi i n k / N} for N in
 // {1, 2, 4, 8, 16}, natural order in and out (radix-2 decimation in time,
-// fully unrolled).  SGN = -1 is the forward transform, +1 the inverse
+// fully unrolled; a butterfly with a twiddle other than 1 or +-i takes six
+// fused multiply-adds).  SGN = -1 is the forward transform, +1 the inverse
 // (unnormalised).  The twiddles inside are the exact angles k*pi/8; their
 // cosines and sines are written out below as float literals.
 #pragma once
@@ -67,9 +68,23 @@ struct Dft {
         Dft<N / 2, SGN>::run(o);
 #pragma unroll
         for (int k = 0; k < N / 2; ++k) {
-            const float2 t = rot16<SGN>(o[k], (16 / N) * k);
-            v[k] = cadd(e[k], t);
-            v[k + N / 2] = csub(e[k], t);
+            const int j = (16 / N) * k;  // in [0, 8): rotation by 1 (j = 0) or +-i (j = 4)
+            if (j == 0 || j == 4) {
+                const float2 t = rot16<SGN>(o[k], j);
+                v[k] = cadd(e[k], t);
+                v[k + N / 2] = csub(e[k], t);
+            } else {
+                // e + w*o as four fused multiply-adds, and e - w*o = 2e - (e + w*o)
+                // as two more (instead of a complex product and four additions)
+                float2 w = unit16(j);
+                if (SGN < 0) w.y = -w.y;
+                const float2 a = o[k], b = e[k];
+                float2 p;
+                p.x = fmaf(a.x, w.x, fmaf(-a.y, w.y, b.x));
+                p.y = fmaf(a.x, w.y, fmaf(a.y, w.x, b.y));
+                v[k] = p;
+                v[k + N / 2] = make_float2(fmaf(2.f, b.x, -p.x), fmaf(2.f, b.y, -p.y));
+            }
         }
     }
 };
