@@ -579,6 +579,123 @@ def run_ours_backward(args, cfg):
         dist.destroy_process_group()
 
 
+def run_ours_1d(args):
+    """The 1D layer (fno_plan_create_1d) on x [B, Cin, L]: forward steps timed
+    like the 2D headline (inputs rotated past L2, CUDA events on the stream,
+    per-kernel breakdown from separate event-armed steps), the oracle's 1D
+    layer timed on the host as the CPU baseline."""
+    import torch
+    import __graft_entry__ as g
+    g.build()
+    from fourier_neural_spectral_gb300 import fnospec
+    B, Cin, Cout, L, m = args.shape1d
+    name = f"1D_B{B}_C{Cin}x{Cout}_L{L}_m{m}"
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = read_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    plan = fnospec.Plan1d(B, Cin, Cout, L, m, args.precision)
+    step_bytes = 4 * B * Cin * L + 4 * B * Cout * L + 8 * Cin * Cout * m
+    nsets = max(1, min(8, -(-3 * L2_BYTES // step_bytes) + 1)) if step_bytes < 3 * L2_BYTES else 1
+    x0 = synth.normal_f32((B, Cin, L), seed=0, stream=1)
+    w0 = synth.uniform_f32((Cin, Cout, m, 2), scale=1.0 / (Cin * Cout), seed=0, stream=2)
+    xs = [torch.from_numpy(x0).to(dev)]
+    ws = [torch.from_numpy(w0).to(dev)]
+    for k in range(1, nsets):
+        xs.append(torch.roll(xs[0], shifts=k, dims=0).contiguous())
+        ws.append((ws[0] * (1.0 + 0.01 * k)).contiguous())
+    ys = [torch.empty((B, Cout, L), dtype=torch.float32, device=dev) for _ in range(nsets)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        j = i % nsets
+        plan.fno_plan_execute(xs[j], ws[j], ys[j], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    nk = plan.launches
+    nbreak = max(3, min(args.steps, 20))
+    evsets = []
+    for _ in range(nbreak):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+        for e in evs:
+            e.record(stream)
+        evsets.append(evs)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    for i in range(nbreak):
+        plan.fno_plan_record_events(evsets[i])
+        step(args.warmup + args.steps + i)
+    plan.fno_plan_record_events(None)
+    torch.cuda.synchronize(dev)
+    if plan.fno_get_device_status() != fnospec.FNO_OK:
+        raise RuntimeError("device status not clean after the 1D steps")
+    ms_per_step = elapsed_ms / args.steps
+    kmean = [statistics.mean(evs[k].elapsed_time(evs[k + 1]) for evs in evsets)
+             for k in range(nk)]
+    kernels = [{"name": plan.kernels[k]["name"], "ms": kmean[k],
+                "gbs": plan.kernels[k]["bytes"] / (kmean[k] * 1e-3) / 1e9,
+                "tflops": plan.kernels[k]["flops"] / (kmean[k] * 1e-3) / 1e12}
+               for k in range(nk)]
+    kdom = int(np.argmax(kmean))
+    fp32_peak = fp32_fma_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)))
+    gemm = 8 * B * Cin * Cout * m
+    t_hbm = step_bytes / (hbm * 1e9)
+    t_roof = max(t_hbm, gemm / (fp32_peak * 1e12))
+    # the direct-DFT transforms' own flops (8 per retained bin and input point
+    # forward, 4 per kept bin and output point inverse) at the fp32 peak
+    dft_flops = 8 * B * Cin * L * m + 4 * B * Cout * L * m
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        nb = max(1, min(B, int(2.5e9 // ((Cin + Cout) * L * m + Cin * Cout * m))))
+        t = time.perf_counter()
+        oracle.spectral_conv1d(x0[:nb].astype(np.float64),
+                               w0.astype(np.float64).view(np.complex128)[..., 0], m)
+        dt = time.perf_counter() - t
+        cpu = {"value": nb / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"oracle 1D layer (numpy direct sums) on {nb} of {B} batch rows",
+               "host": platform.machine(), "host_cores": os.cpu_count()}
+    line = {
+        "metric": "FNO 1D spectral-conv samples/s; % of HBM roofline", "value":
+        B * args.steps / (elapsed_ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": name, "B": B, "Cin": Cin, "Cout": Cout, "L": L, "m": m,
+                   "precision": args.precision, "l2": f"inputs rotate over {nsets} buffer sets"},
+        "roofline": {"kernel": kernels[kdom]["name"], "bound": "hbm",
+                     "achieved": kernels[kdom]["gbs"], "peak": hbm, "unit": "GB/s",
+                     "frac": kernels[kdom]["gbs"] / hbm, "traffic": None,
+                     "peak_kind": f"{peak_kind} (hbm_gbs)"},
+        "layer_roofline": {"bytes_per_step": step_bytes, "t_roof_us": t_roof * 1e6,
+                           "t_step_us": ms_per_step * 1e3, "frac": t_roof / (ms_per_step * 1e-3),
+                           "dft_flops_per_step": dft_flops,
+                           "dft_t_at_fp32_peak_us": dft_flops / (fp32_peak * 1e12) * 1e6},
+        "kernels": kernels, "plan": plan.description, "cpu_baseline": cpu,
+        "gpu_launches": nk * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def parse_ints(text: str, n: int):
+    vals = [int(v) for v in text.split(",")]
+    if len(vals) != n:
+        raise SystemExit(f"expected {n} comma-separated integers, got {text!r}")
+    return vals
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -589,13 +706,27 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pass", dest="pass_", default="forward",
-                    choices=["forward", "backward", "block"],
-                    help="forward (the headline), the layer's backward, or one FNO block "
-                         "(layer + pointwise branch + bias + GELU); fp32")
+                    choices=["forward", "backward", "block", "layer1d"],
+                    help="forward (the headline), the layer's backward, one FNO block "
+                         "(layer + pointwise branch + bias + GELU), or the 1D layer")
+    ap.add_argument("--shape", default=None,
+                    help="B,Cin,Cout,H,W,m1,m2: a workload other than the named configs "
+                         "(any H, W in [2, 4096]); x ~ N(0,1), w ~ U[0,1)/(Cin*Cout)")
+    ap.add_argument("--shape1d", default="64,64,64,4096,64",
+                    help="B,Cin,Cout,L,m of the 1D layer (--pass layer1d)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    cfg = synth.CONFIGS[args.config]
+    if args.pass_ == "layer1d":
+        args.shape1d = parse_ints(args.shape1d, 5)
+        run_ours_1d(args)
+        return
+    if args.shape:
+        B, Cin, Cout, H, W, m1, m2 = parse_ints(args.shape, 7)
+        cfg = synth.LayerConfig(f"B{B}_C{Cin}x{Cout}_{H}x{W}_m{m1}x{m2}", B, Cin, Cout, H, W,
+                                m1, m2)
+    else:
+        cfg = synth.CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, cfg)
     elif args.pass_ == "backward":

@@ -26,41 +26,171 @@ constexpr int kRowsPerWarp = 4;  // column steps: output rows (or h) per warp
 
 __device__ __forceinline__ int kr(int r, int H, int m1) { return r < m1 ? r : H - 2 * m1 + r; }
 
-// One CTA per RB consecutive rows (of all planes, flattened); rows and the
-// twiddle table in shared memory; warp j computes the (row, k2) outputs j,
-// j + 8, ..., lanes striding over w, then a shuffle reduction.
-__global__ void __launch_bounds__(kDftThreads)
-dft_rows_fwd_kernel(const float* __restrict__ x, float2* __restrict__ T, long long nrows, int W,
-                    int m2, int RB, float out_scale, const float2* __restrict__ tw_w) {
-    extern __shared__ float2 dsm[];
-    float2* tw = dsm;                                  // [W]
-    float* xs = reinterpret_cast<float*>(dsm + W);     // [RB][W]
-    const long long row0 = (long long)blockIdx.x * RB;
-    const int nr = (int)std::min<long long>(RB, nrows - row0);
-    for (int i = threadIdx.x; i < W; i += kDftThreads) tw[i] = tw_w[i];
-    for (int i = threadIdx.x; i < nr * W; i += kDftThreads) xs[i] = __ldg(&x[row0 * W + i]);
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int job = warp; job < nr * m2; job += kWarps) {
-        const int r = job / m2, k2 = job - r * m2;
-        const float* xr = xs + r * W;
-        float re = 0.f, im = 0.f;
-        int idx = (int)(((long long)k2 * lane) % W);
-        const int step = (int)(((long long)k2 * 32) % W);
-        for (int w = lane; w < W; w += 32) {
-            const float v = xr[w];
-            const float2 t = tw[idx];           // e^{+2 pi i k2 w / W}
-            re = fmaf(v, t.x, re);
-            im = fmaf(-v, t.y, im);             // conjugate: forward sign
-            idx += step;
-            if (idx >= W) idx -= W;
-        }
+// The row steps as real matrix products over all rows of all planes (M rows):
+//   forward  C[row][n] = sum_w x[row][w] F[w][n],  n = 2*k2 + c,  N = 2*m2:
+//            F[w][2k2] = cos(2 pi k2 w / W), F[w][2k2 + 1] = -sin(2 pi k2 w / W),
+//            so C is T (k2 < m2 interleaved as re, im) and K = W;
+//   inverse  C[row][w] = scale * sum_j V'[row][j] G[j][w],  j = 2*k2 + c, K = 2*m2:
+//            V'[row][j] = c(k2) * (re or im of V[row][k2]),
+//            G[2k2][w] = cos(2 pi k2 w / W), G[2k2 + 1][w] = -sin(2 pi k2 w / W),
+//            the real part of sum_k2 c(k2) V[k2] e^{+2 pi i k2 w / W}, N = W.
+// The twiddle operand is filled per K chunk from the table e^{+2 pi i j / W} at
+// the exact index (k2 * w) mod W, kept incrementally (one division per thread
+// per launch).  CTA: 256 threads, BM x BN outputs, each thread TM rows x 8
+// columns in registers; per K step one shared-memory float4 of A (TM = 4) and
+// two of twiddles feed TM * 8 fused multiply-adds.  The chunks are double
+// buffered: the next chunk of A is loaded into registers and its twiddles are
+// formed while the current one is multiplied.  With few output tiles the K
+// range is split over CTAs (ksplit > 1) that add their partial sums into C,
+// which the launcher has zeroed.
+constexpr int kGT = 256;  // threads per CTA
+constexpr int kGBK = 16;  // K chunk
+constexpr int kGTN = 8;   // columns per thread
+
+template <int BN, int TM>
+struct RowGemm {
+    static constexpr int NX = BN / kGTN;  // threads along N
+    static constexpr int NY = kGT / NX;   // threads along M
+    static constexpr int BM = NY * TM;
+    static constexpr int AS = BM + 4;     // As row stride (floats)
+    static constexpr int AE = BM * kGBK / kGT;  // A elements per thread per chunk
+    static constexpr int BE = BN * kGBK / kGT;  // twiddle elements per thread per chunk
+    static constexpr int KS = kGT / BN;         // twiddle row step between a thread's elements
+    // CTAs per SM the registers are sized for (<64, 2>: 64 registers; TM = 4:
+    // at most 128)
+    static constexpr int MinBlocks = TM == 2 ? 4 : 2;
+};
+
+template <int BN, int TM, bool FWD>
+__global__ void __launch_bounds__(kGT, (RowGemm<BN, TM>::MinBlocks))
+dft_rows_gemm_kernel(const float* __restrict__ A, float* __restrict__ C, long long M, int K,
+                     int N, int W, float scale, const float2* __restrict__ tw, int ksplit,
+                     int kper) {
+    using G = RowGemm<BN, TM>;
+    __shared__ __align__(16) float As[2][kGBK][G::AS];
+    __shared__ __align__(16) float Bs[2][kGBK][BN];
+    const int ntiles = (N + BN - 1) / BN;
+    const int ks = blockIdx.x % ksplit;
+    const int tile = blockIdx.x / ksplit;
+    const long long row0 = (long long)(tile / ntiles) * G::BM;
+    const int n0 = (tile % ntiles) * BN;
+    const int kbeg = ks * kper, kend = min(K, kbeg + kper);
+    const int tid = threadIdx.x, tx = tid % G::NX, ty = tid / G::NX;
+
+    // this thread's A elements: rows tid / 16 + 16 i, column tid % 16 of a chunk
+    const int akk = tid % kGBK, ar = tid / kGBK;
+    // this thread's twiddle elements: column nn, rows kr + KS * i of a chunk
+    const int nn = tid % BN, kr = tid / BN;
+    const int n = n0 + nn;
+    // twiddle index (freq * pos) mod W at the chunk start, its step between the
+    // thread's elements and its advance per chunk
+    int tbase, tstep, tadv;
+    bool imag;
+    if (FWD) {  // freq = n / 2 fixed, pos = k
+        const int freq = n >> 1;
+        imag = n & 1;
+        tbase = (int)(((long long)freq * (kbeg + kr)) % W);
+        tstep = (int)(((long long)freq * G::KS) % W);
+        tadv = (int)(((long long)freq * kGBK) % W);
+    } else {    // pos = n fixed, freq = k / 2 (the parity of k is the thread's)
+        imag = kr & 1;
+        const int pos = n < N ? n : 0;
+        tbase = (int)(((long long)((kbeg + kr) >> 1) * pos) % W);
+        tstep = (int)(((long long)(G::KS / 2) * pos) % W);
+        tadv = (int)(((long long)(kGBK / 2) * pos) % W);
+    }
+    const auto add_mod = [W](int a, int b) { a += b; return a >= W ? a - W : a; };
+
+    float ra[G::AE];
+    const auto load_a = [&](int k0) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            re += __shfl_xor_sync(0xffffffffu, re, o);
-            im += __shfl_xor_sync(0xffffffffu, im, o);
+        for (int i = 0; i < G::AE; ++i) {
+            const long long row = row0 + ar + (kGT / kGBK) * i;
+            const int k = k0 + akk;
+            float v = 0.f;
+            if (row < M && k < kend) {
+                v = __ldg(&A[row * K + k]);
+                if (!FWD) {
+                    const int k2 = k >> 1;
+                    if (k2 != 0 && 2 * k2 != W) v += v;  // c(k2) = 2
+                }
+            }
+            ra[i] = v;
         }
-        if (lane == 0) T[(row0 + r) * m2 + k2] = make_float2(re * out_scale, im * out_scale);
+    };
+    const auto store_chunk = [&](int buf, int k0) {
+#pragma unroll
+        for (int i = 0; i < G::AE; ++i) As[buf][akk][ar + (kGT / kGBK) * i] = ra[i];
+        int idx = tbase;
+#pragma unroll
+        for (int i = 0; i < G::BE; ++i) {
+            const int k = k0 + kr + G::KS * i;
+            float v = 0.f;
+            if (k < kend && n < N) {
+                const float2 t = __ldg(&tw[idx]);
+                v = imag ? -t.y : t.x;
+            }
+            Bs[buf][kr + G::KS * i][nn] = v;
+            idx = add_mod(idx, tstep);
+        }
+        tbase = add_mod(tbase, tadv);
+    };
+
+    float acc[TM][kGTN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < kGTN; ++j) acc[i][j] = 0.f;
+
+    load_a(kbeg);
+    store_chunk(0, kbeg);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = kbeg; k0 < kend; k0 += kGBK) {
+        const bool more = k0 + kGBK < kend;
+        if (more) load_a(k0 + kGBK);
+#pragma unroll
+        for (int kk = 0; kk < kGBK; ++kk) {
+            float av[TM];
+            if constexpr (TM == 4) {
+                const float4 a = *reinterpret_cast<const float4*>(&As[buf][kk][ty * TM]);
+                av[0] = a.x; av[1] = a.y; av[2] = a.z; av[3] = a.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < TM; ++i) av[i] = As[buf][kk][ty * TM + i];
+            }
+            float bv[kGTN];
+            if constexpr (FWD) {  // columns tx*8 .. tx*8 + 7
+                const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * kGTN]);
+                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * kGTN + 4]);
+                bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+                bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+            } else {              // columns tx + NX*j: stores of 8 lanes are contiguous
+#pragma unroll
+                for (int j = 0; j < kGTN; ++j) bv[j] = Bs[buf][kk][tx + G::NX * j];
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < kGTN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        if (more) store_chunk(buf ^ 1, k0 + kGBK);
+        __syncthreads();
+        buf ^= 1;
+    }
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const long long row = row0 + ty * TM + i;
+        if (row >= M) break;
+        float* Cr = C + row * N;
+#pragma unroll
+        for (int j = 0; j < kGTN; ++j) {
+            const int nj = n0 + (FWD ? tx * kGTN + j : tx + G::NX * j);
+            if (nj < N) {
+                if (ksplit == 1) Cr[nj] = acc[i][j] * scale;
+                else atomicAdd(&Cr[nj], acc[i][j] * scale);
+            }
+        }
     }
 }
 
@@ -142,41 +272,60 @@ dft_cols_inv_kernel(const float2* __restrict__ Z, float2* __restrict__ T, long l
     }
 }
 
-// Inverse rows: CTA = RB consecutive rows of V (all planes flattened), the row
-// values c(k2) V[k2] and the twiddle table in shared memory; thread per output
-// w (strided), sum over k2 of Re(c V e^{+2 pi i k2 w / W}).
-__global__ void __launch_bounds__(kDftThreads)
-dft_rows_inv_kernel(const float2* __restrict__ T, float* __restrict__ y, long long nrows, int W,
-                    int m2, int RB, float scale, const float2* __restrict__ tw_w) {
-    extern __shared__ float2 dsm[];
-    float2* tw = dsm;            // [W]
-    float2* vs = dsm + W;        // [RB][m2], times c(k2)
-    const long long row0 = (long long)blockIdx.x * RB;
-    const int nr = (int)std::min<long long>(RB, nrows - row0);
-    for (int i = threadIdx.x; i < W; i += kDftThreads) tw[i] = tw_w[i];
-    for (int i = threadIdx.x; i < nr * m2; i += kDftThreads) {
-        const int k2 = i % m2;
-        const float c = (k2 == 0 || 2 * k2 == W) ? 1.f : 2.f;
-        vs[i] = cscale(__ldg(&T[row0 * m2 + i]), c);
+// One row step as the matrix product above: M rows, contraction length K, N
+// outputs per row.  The forward takes 32-column tiles of 256 rows for narrow
+// outputs (2*m2 <= 32), else 64 columns by 128 rows, or by 64 rows when that
+// would leave fewer than two CTAs per SM; the inverse always 64 by 64.  If the tiles still number fewer
+// than two per SM, the K range is split over CTAs (chunks of at least 64) whose
+// partial sums are added into C after it is zeroed; their order of addition
+// varies from run to run.
+template <bool FWD>
+cudaError_t launch_rows_gemm(const float* A, float* C, long long M, int K, int N, int W,
+                             float scale, const float2* tw, cudaStream_t s) {
+    constexpr long long kWant = 2 * 152;
+    const auto tiles = [&](int bn, int bm) {
+        return ((M + bm - 1) / bm) * (long long)((N + bn - 1) / bn);
+    };
+    int cfg;  // 0: <32, 4>, 1: <64, 4>, 2: <64, 2>
+    long long t;
+    if (!FWD) {
+        // the inverse's K (2*m2) is short and its output (y) large: the
+        // 64-register tile at four CTAs per SM
+        cfg = 2;
+        t = tiles(64, RowGemm<64, 2>::BM);
+    } else if (N <= 32) {
+        cfg = 0;
+        t = tiles(32, RowGemm<32, 4>::BM);
+    } else if (tiles(64, RowGemm<64, 4>::BM) >= kWant) {
+        cfg = 1;
+        t = tiles(64, RowGemm<64, 4>::BM);
+    } else {
+        cfg = 2;
+        t = tiles(64, RowGemm<64, 2>::BM);
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < nr * W; i += kDftThreads) {
-        const int r = i / W, w = i - r * W;
-        const float2* v = vs + r * m2;
-        float acc = 0.f;
-        int idx = 0;
-        for (int k2 = 0; k2 < m2; ++k2) {
-            const float2 t = tw[idx];  // e^{+2 pi i k2 w / W}
-            acc = fmaf(v[k2].x, t.x, acc);
-            acc = fmaf(-v[k2].y, t.y, acc);
-            idx += w;
-            if (idx >= W) idx -= W;
-        }
-        y[(row0 + r) * W + w] = acc * scale;
+    int ksplit = 1;
+    if (t < kWant && K >= 2 * 64) {
+        ksplit = (int)std::min<long long>((kWant + t - 1) / t, K / 64);
     }
+    int kper = (K + ksplit - 1) / ksplit;
+    kper = (kper + kGBK - 1) / kGBK * kGBK;
+    ksplit = (K + kper - 1) / kper;
+    if (ksplit > 1) {
+        cudaError_t e = cudaMemsetAsync(C, 0, sizeof(float) * (size_t)M * N, s);
+        if (e != cudaSuccess) return e;
+    }
+    const unsigned grid = (unsigned)(t * ksplit);
+    if (cfg == 0)
+        dft_rows_gemm_kernel<32, 4, FWD><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
+                                                              ksplit, kper);
+    else if (cfg == 1)
+        dft_rows_gemm_kernel<64, 4, FWD><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
+                                                              ksplit, kper);
+    else
+        dft_rows_gemm_kernel<64, 2, FWD><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
+                                                              ksplit, kper);
+    return cudaGetLastError();
 }
-
-int rows_per_cta(int W) { return std::max(1, std::min(16, 16384 / W)); }
 
 }  // namespace
 }  // namespace fno
@@ -188,27 +337,13 @@ bool dft_path(int H, int W) {
     return !pow2(H) || !pow2(W);
 }
 
-cudaError_t stages_dft_init() {
-    // largest requests: W = 4096 (4 rows per CTA): 32 KB of twiddles + 64 KB of x
-    // rows, or 4 rows of m2 <= 2049 values
-    const int fwd = (int)(sizeof(float2) * 4096 + sizeof(float) * 4 * 4096);
-    const int inv = (int)(sizeof(float2) * 4096 + sizeof(float2) * 4 * 2049);
-    cudaError_t e = cudaFuncSetAttribute(dft_rows_fwd_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, fwd);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(dft_rows_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 inv);
-    return e;
-}
+cudaError_t stages_dft_init() { return cudaSuccess; }  // static shared memory only
 
 cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, float2* T,
                                cudaStream_t s, fno_launch_ctx* ctx) {
     const long long planes = (long long)p.B * p.Cin, nrows = planes * p.H;
-    const int RB = rows_per_cta(p.W);
-    const size_t smem = sizeof(float2) * p.W + sizeof(float) * (size_t)RB * p.W;
-    dft_rows_fwd_kernel<<<(unsigned)((nrows + RB - 1) / RB), kDftThreads, smem, s>>>(
-        x, T, nrows, p.W, p.m2, RB, 1.f, p.tw_w);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_rows_gemm<true>(x, reinterpret_cast<float*>(T), nrows, p.W, 2 * p.m2,
+                                           p.W, 1.f, p.tw_w, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     if (e != cudaSuccess) return e;
     const long long jobs = planes * ((2 * p.m1 + kRowsPerWarp - 1) / kRowsPerWarp);
@@ -228,11 +363,8 @@ cudaError_t launch_inverse_dft(const fno_plan_s& p, const float2* Z, float* y, f
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     if (e != cudaSuccess) return e;
-    const int RB = rows_per_cta(p.W);
-    const size_t smem = sizeof(float2) * p.W + sizeof(float2) * (size_t)RB * p.m2;
-    dft_rows_inv_kernel<<<(unsigned)((nrows + RB - 1) / RB), kDftThreads, smem, s>>>(
-        T, y, nrows, p.W, p.m2, RB, p.scale, p.tw_w);
-    e = cudaGetLastError();
+    e = launch_rows_gemm<false>(reinterpret_cast<const float*>(T), y, nrows, 2 * p.m2, p.W, p.W,
+                                p.scale, p.tw_w, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
@@ -242,11 +374,8 @@ cudaError_t launch_inverse_dft(const fno_plan_s& p, const float2* Z, float* y, f
 cudaError_t launch_forward_1d(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s,
                               fno_launch_ctx* ctx) {
     const long long nrows = (long long)p.B * p.Cin;
-    const int RB = rows_per_cta(p.W);
-    const size_t smem = sizeof(float2) * p.W + sizeof(float) * (size_t)RB * p.W;
-    dft_rows_fwd_kernel<<<(unsigned)((nrows + RB - 1) / RB), kDftThreads, smem, s>>>(
-        x, X, nrows, p.W, p.m2, RB, p.scale, p.tw_w);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_rows_gemm<true>(x, reinterpret_cast<float*>(X), nrows, p.W, 2 * p.m2,
+                                           p.W, p.scale, p.tw_w, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
@@ -254,11 +383,8 @@ cudaError_t launch_forward_1d(const fno_plan_s& p, const float* x, float2* X, cu
 cudaError_t launch_inverse_1d(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s,
                               fno_launch_ctx* ctx) {
     const long long nrows = (long long)p.B * p.Cout;
-    const int RB = rows_per_cta(p.W);
-    const size_t smem = sizeof(float2) * p.W + sizeof(float2) * (size_t)RB * p.m2;
-    dft_rows_inv_kernel<<<(unsigned)((nrows + RB - 1) / RB), kDftThreads, smem, s>>>(
-        Z, y, nrows, p.W, p.m2, RB, p.scale, p.tw_w);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_rows_gemm<false>(reinterpret_cast<const float*>(Z), y, nrows,
+                                            2 * p.m2, p.W, p.W, p.scale, p.tw_w, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
