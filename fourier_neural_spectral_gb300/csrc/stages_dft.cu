@@ -11,7 +11,10 @@
 // H - 2*m1 + r otherwise, c = 1 for k2 = 0 and k2 = W/2 and 2 otherwise (TurboFNO
 // page, sections 2.2 and 3.1; the half-spectrum width W/2 + 1 of the FFT
 // operator-optimisation page, section 2.2).  Twiddles come from the plan's
-// tables e^{+2 pi i j / N}, indexed by the exact integer (k * n) mod N.
+// tables e^{+2 pi i j / N}, indexed by the exact integer (k * n) mod N.  Each
+// step is a dense product with a twiddle matrix (the rows over all rows of all
+// planes, the columns batched over planes), computed by register-tiled fp32
+// kernels below.
 #include <algorithm>
 
 #include "common.cuh"
@@ -20,11 +23,6 @@
 namespace fno {
 namespace {
 
-constexpr int kDftThreads = 256;
-constexpr int kWarps = kDftThreads / 32;
-constexpr int kRowsPerWarp = 4;  // column steps: output rows (or h) per warp
-
-__device__ __forceinline__ int kr(int r, int H, int m1) { return r < m1 ? r : H - 2 * m1 + r; }
 
 // The row steps as real matrix products over all rows of all planes (M rows):
 //   forward  C[row][n] = sum_w x[row][w] F[w][n],  n = 2*k2 + c,  N = 2*m2:
@@ -194,80 +192,124 @@ dft_rows_gemm_kernel(const float* __restrict__ A, float* __restrict__ C, long lo
     }
 }
 
-// Forward columns: warp = (plane, 4 consecutive retained rows r), lanes over
-// k2 (in blocks of 32); per h one coalesced read of T[q][h][k2] serves the 4
-// rows, whose twiddles are warp-uniform.
-__global__ void __launch_bounds__(kDftThreads)
-dft_cols_fwd_kernel(const float2* __restrict__ T, float2* __restrict__ X, long long planes, int H,
-                    int m1, int m2, float scale, const float2* __restrict__ tw_h) {
-    const int lane = threadIdx.x & 31;
-    const int R = 2 * m1, rg = (R + kRowsPerWarp - 1) / kRowsPerWarp;
-    const long long job = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (job >= planes * rg) return;
-    const long long q = job / rg;
-    const int r0 = (int)(job - q * rg) * kRowsPerWarp;
-    const float2* Tq = T + q * H * m2;
-    for (int kb = 0; kb < m2; kb += 32) {
-        const int k2 = kb + lane;
-        float2 acc[kRowsPerWarp];
-        int k1[kRowsPerWarp], idx[kRowsPerWarp];  // idx = (k1 * h) mod H, stepped with h
-#pragma unroll
-        for (int j = 0; j < kRowsPerWarp; ++j) {
-            acc[j] = make_float2(0.f, 0.f);
-            k1[j] = r0 + j < R ? kr(r0 + j, H, m1) : 0;
-            idx[j] = 0;
-        }
-        for (int h = 0; h < H; ++h) {
-            const float2 v = k2 < m2 ? __ldg(&Tq[(size_t)h * m2 + k2]) : make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < kRowsPerWarp; ++j) {
-                float2 t = __ldg(&tw_h[idx[j]]);
-                t.y = -t.y;  // e^{-2 pi i k1 h / H}
-                cmac(acc[j], v, t);
-                idx[j] += k1[j];
-                if (idx[j] >= H) idx[j] -= H;
-            }
-        }
-        if (k2 < m2) {
-#pragma unroll
-            for (int j = 0; j < kRowsPerWarp; ++j)
-                if (r0 + j < R) X[(q * R + r0 + j) * m2 + k2] = cscale(acc[j], scale);
-        }
-    }
-}
+// The column steps as complex matrix products batched over the planes q, with
+// the columns c = (q, k2) of all planes side by side:
+//   forward  X_q[r][k2] = s * sum_h F[r][h] T_q[h][k2],  F[r][h] = e^{-2 pi i k1(r) h / H},
+//   inverse  T_q[h][k2] = sum_r G[h][r] Z_q[r][k2],      G[h][r] = e^{+2 pi i k1(r) h / H},
+// i.e. C[m][c] = alpha * sum_k A[m][k] B[k][c], with B[k][(q, k2)] at
+// (q*KB + k)*m2 + k2 and C[m][(q, k2)] at (q*MC + m)*m2 + k2.  A is formed per K
+// chunk from the table e^{+2 pi i j / H} (forward: index kept incrementally).
+// CTA: 128 threads, 32 rows x 32 complex columns; each thread 4 rows x 2
+// columns (columns tx and tx + 16, so that 16 lanes store 128 contiguous
+// bytes); per K step two float4 of A and two float2 of B feed 32 fused
+// multiply-adds.  Chunks of 16 are double buffered.
+constexpr int kCT = 128;   // threads
+constexpr int kCBK = 16;   // K chunk
+constexpr int kCBM = 32;   // rows per CTA
+constexpr int kCBN = 32;   // complex columns per CTA
 
-// Inverse columns: warp = (plane, 4 consecutive h), lanes over k2; per retained
-// row r one coalesced read of Z[q][r][k2] serves the 4 h.
-__global__ void __launch_bounds__(kDftThreads)
-dft_cols_inv_kernel(const float2* __restrict__ Z, float2* __restrict__ T, long long planes, int H,
-                    int m1, int m2, const float2* __restrict__ tw_h) {
-    const int lane = threadIdx.x & 31;
-    const int R = 2 * m1, hg = (H + kRowsPerWarp - 1) / kRowsPerWarp;
-    const long long job = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (job >= planes * hg) return;
-    const long long q = job / hg;
-    const int h0 = (int)(job - q * hg) * kRowsPerWarp;
-    const float2* Zq = Z + q * R * m2;
-    for (int kb = 0; kb < m2; kb += 32) {
-        const int k2 = kb + lane;
-        float2 acc[kRowsPerWarp];
+template <bool FWD>
+__global__ void __launch_bounds__(kCT)
+dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst, int M, int K,
+                     long long ncols, int m2, int KB, int MC, int H, int m1, float alpha,
+                     const float2* __restrict__ tw_h) {
+    __shared__ __align__(16) float2 As[2][kCBK][kCBM];
+    __shared__ __align__(16) float2 Bs[2][kCBK][kCBN];
+    const int mtiles = (M + kCBM - 1) / kCBM;
+    const int m0 = (int)(blockIdx.x % mtiles) * kCBM;
+    const long long c0 = (long long)(blockIdx.x / mtiles) * kCBN;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;  // ty < 8: rows ty*4 .. +3
+
+    // loader roles: B column cc = tid % 32, K rows tid / 32 + 4 i; A row mm = tid % 32,
+    // K rows tid / 32 + 4 i
+    const int lc = tid % 32, lk = tid / 32;
+    const long long bc = c0 + lc;
+    const bool bvalid = bc < ncols;
+    const long long bq = bvalid ? bc / m2 : 0;
+    const int bk2 = bvalid ? (int)(bc - bq * m2) : 0;
+    const float2* Bcol = Bsrc + (size_t)bq * KB * m2 + bk2;
+    const int am = m0 + lc;
+    const bool avalid = am < M;
+    const auto k1_of = [H, m1](int r) { return r < m1 ? r : H - 2 * m1 + r; };
+    // forward: A[m][k] = conj(tab[(k1(m) * k) mod H]), k1 fixed per thread
+    const int ak1 = FWD && avalid ? k1_of(am) : 0;
+    int abase = FWD ? (int)(((long long)ak1 * lk) % H) : 0;
+    const int astep = FWD ? (int)(((long long)ak1 * 4) % H) : 0;
+    const int aadv = FWD ? (int)(((long long)ak1 * kCBK) % H) : 0;
+
+    float2 rb[4];
+    const auto load_b = [&](int k0) {
 #pragma unroll
-        for (int j = 0; j < kRowsPerWarp; ++j) acc[j] = make_float2(0.f, 0.f);
-        for (int r = 0; r < R; ++r) {
-            const float2 v = k2 < m2 ? __ldg(&Zq[(size_t)r * m2 + k2]) : make_float2(0.f, 0.f);
-            const int k1 = kr(r, H, m1);
-            int idx = (int)(((long long)k1 * h0) % H);  // (k1 * h) mod H for h = h0 + j
+        for (int i = 0; i < 4; ++i) {
+            const int k = k0 + lk + 4 * i;
+            rb[i] = bvalid && k < K ? __ldg(&Bcol[(size_t)k * m2]) : make_float2(0.f, 0.f);
+        }
+    };
+    const auto store_chunk = [&](int buf, int k0) {
 #pragma unroll
-            for (int j = 0; j < kRowsPerWarp; ++j) {
-                cmac(acc[j], v, __ldg(&tw_h[idx]));  // e^{+2 pi i k1 h / H}
-                idx += k1;
+        for (int i = 0; i < 4; ++i) Bs[buf][lk + 4 * i][lc] = rb[i];
+        int idx = abase;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = k0 + lk + 4 * i;
+            float2 a = make_float2(0.f, 0.f);
+            if (avalid && k < K) {
+                if (FWD) {
+                    a = __ldg(&tw_h[idx]);
+                    a.y = -a.y;
+                } else {
+                    a = __ldg(&tw_h[(int)(((long long)k1_of(k) * am) % H)]);
+                }
+            }
+            As[buf][lk + 4 * i][lc] = a;
+            if (FWD) {
+                idx += astep;
                 if (idx >= H) idx -= H;
             }
         }
-        if (k2 < m2) {
+        if (FWD) {
+            abase += aadv;
+            if (abase >= H) abase -= H;
+        }
+    };
+
+    float2 acc[4][2];
 #pragma unroll
-            for (int j = 0; j < kRowsPerWarp; ++j)
-                if (h0 + j < H) T[(q * H + h0 + j) * m2 + k2] = acc[j];
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
+
+    load_b(0);
+    store_chunk(0, 0);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = 0; k0 < K; k0 += kCBK) {
+        const bool more = k0 + kCBK < K;
+        if (more) load_b(k0 + kCBK);
+#pragma unroll
+        for (int kk = 0; kk < kCBK; ++kk) {
+            const float4 a01 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+            const float4 a23 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4 + 2]);
+            const float2 av[4] = {make_float2(a01.x, a01.y), make_float2(a01.z, a01.w),
+                                  make_float2(a23.x, a23.y), make_float2(a23.z, a23.w)};
+            const float2 bv[2] = {Bs[buf][kk][tx], Bs[buf][kk][tx + 16]};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) cmac(acc[i][j], av[i], bv[j]);
+        }
+        if (more) store_chunk(buf ^ 1, k0 + kCBK);
+        __syncthreads();
+        buf ^= 1;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const long long c = c0 + tx + 16 * j;
+        if (c >= ncols) continue;
+        const long long q = c / m2;
+        const int k2 = (int)(c - q * m2);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = m0 + ty * 4 + i;
+            if (m < M) Cdst[((size_t)q * MC + m) * m2 + k2] = cscale(acc[i][j], alpha);
         }
     }
 }
@@ -327,6 +369,17 @@ cudaError_t launch_rows_gemm(const float* A, float* C, long long M, int K, int N
     return cudaGetLastError();
 }
 
+template <bool FWD>
+cudaError_t launch_cols_gemm(const float2* B, float2* C, int M, int K, long long planes, int m2,
+                             int KB, int MC, int H, int m1, float alpha, const float2* tw_h,
+                             cudaStream_t s) {
+    const long long ncols = planes * m2;
+    const long long grid = (long long)((M + kCBM - 1) / kCBM) * ((ncols + kCBN - 1) / kCBN);
+    dft_cols_gemm_kernel<FWD><<<(unsigned)grid, kCT, 0, s>>>(B, C, M, K, ncols, m2, KB, MC, H,
+                                                             m1, alpha, tw_h);
+    return cudaGetLastError();
+}
+
 }  // namespace
 }  // namespace fno
 
@@ -346,10 +399,8 @@ cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, f
                                            p.W, 1.f, p.tw_w, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     if (e != cudaSuccess) return e;
-    const long long jobs = planes * ((2 * p.m1 + kRowsPerWarp - 1) / kRowsPerWarp);
-    dft_cols_fwd_kernel<<<(unsigned)((jobs + kWarps - 1) / kWarps), kDftThreads, 0, s>>>(
-        T, X, planes, p.H, p.m1, p.m2, p.scale, p.tw_h);
-    e = cudaGetLastError();
+    e = launch_cols_gemm<true>(T, X, 2 * p.m1, p.H, planes, p.m2, p.H, 2 * p.m1, p.H, p.m1,
+                               p.scale, p.tw_h, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
@@ -357,10 +408,8 @@ cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, f
 cudaError_t launch_inverse_dft(const fno_plan_s& p, const float2* Z, float* y, float2* T,
                                cudaStream_t s, fno_launch_ctx* ctx) {
     const long long planes = (long long)p.B * p.Cout, nrows = planes * p.H;
-    const long long jobs = planes * ((p.H + kRowsPerWarp - 1) / kRowsPerWarp);
-    dft_cols_inv_kernel<<<(unsigned)((jobs + kWarps - 1) / kWarps), kDftThreads, 0, s>>>(
-        Z, T, planes, p.H, p.m1, p.m2, p.tw_h);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_cols_gemm<false>(Z, T, p.H, 2 * p.m1, planes, p.m2, 2 * p.m1, p.H,
+                                            p.H, p.m1, 1.f, p.tw_h, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     if (e != cudaSuccess) return e;
     e = launch_rows_gemm<false>(reinterpret_cast<const float*>(T), y, nrows, 2 * p.m2, p.W, p.W,
