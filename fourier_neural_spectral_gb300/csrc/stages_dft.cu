@@ -35,8 +35,11 @@ namespace {
 // The twiddle operand is filled per K chunk from the table e^{+2 pi i j / W} at
 // the exact index (k2 * w) mod W, kept incrementally (one division per thread
 // per launch).  CTA: 256 threads, BM x BN outputs, each thread TM rows x 8
-// columns in registers; per K step one shared-memory float4 of A (TM = 4) and
-// two of twiddles feed TM * 8 fused multiply-adds.  The chunks are double
+// columns in registers: grouped (columns tx*4 .. +3 and BN/2 + tx*4 .. +3,
+// stored as float4 when rows start on 16 bytes) or interleaved (columns
+// tx + NX*j, so that eight lanes store 32 contiguous bytes); per K step one
+// shared-memory float4 of A (TM = 4) and two float4 of twiddles (grouped) feed
+// TM * 8 fused multiply-adds.  The chunks are double
 // buffered: the next chunk of A is loaded into registers and its twiddles are
 // formed while the current one is multiplied.  With few output tiles the K
 // range is split over CTAs (ksplit > 1) that add their partial sums into C,
@@ -59,7 +62,7 @@ struct RowGemm {
     static constexpr int MinBlocks = TM == 2 ? 4 : 2;
 };
 
-template <int BN, int TM, bool FWD>
+template <int BN, int TM, bool FWD, bool GROUPED>
 __global__ void __launch_bounds__(kGT, (RowGemm<BN, TM>::MinBlocks))
 dft_rows_gemm_kernel(const float* __restrict__ A, float* __restrict__ C, long long M, int K,
                      int N, int W, float scale, const float2* __restrict__ tw, int ksplit,
@@ -158,12 +161,13 @@ dft_rows_gemm_kernel(const float* __restrict__ A, float* __restrict__ C, long lo
                 for (int i = 0; i < TM; ++i) av[i] = As[buf][kk][ty * TM + i];
             }
             float bv[kGTN];
-            if constexpr (FWD) {  // columns tx*8 .. tx*8 + 7
-                const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * kGTN]);
-                const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * kGTN + 4]);
+            if constexpr (GROUPED) {  // columns tx*4 .. +3 and BN/2 + tx*4 .. +3
+                const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+                const float4 b1 =
+                    *reinterpret_cast<const float4*>(&Bs[buf][kk][BN / 2 + tx * 4]);
                 bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
                 bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
-            } else {              // columns tx + NX*j: stores of 8 lanes are contiguous
+            } else {                  // columns tx + NX*j
 #pragma unroll
                 for (int j = 0; j < kGTN; ++j) bv[j] = Bs[buf][kk][tx + G::NX * j];
             }
@@ -176,17 +180,30 @@ dft_rows_gemm_kernel(const float* __restrict__ A, float* __restrict__ C, long lo
         __syncthreads();
         buf ^= 1;
     }
+    // rows of C start on 16 bytes when N % 4 == 0 (C itself is 256-byte aligned)
+    const bool vec = GROUPED && ksplit == 1 && (N & 3) == 0;
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
         const long long row = row0 + ty * TM + i;
         if (row >= M) break;
         float* Cr = C + row * N;
 #pragma unroll
-        for (int j = 0; j < kGTN; ++j) {
-            const int nj = n0 + (FWD ? tx * kGTN + j : tx + G::NX * j);
-            if (nj < N) {
-                if (ksplit == 1) Cr[nj] = acc[i][j] * scale;
-                else atomicAdd(&Cr[nj], acc[i][j] * scale);
+        for (int g = 0; g < 2; ++g) {
+            const int nb = n0 + (GROUPED ? g * (BN / 2) + tx * 4 : 0);
+            if (vec && nb + 3 < N) {
+                *reinterpret_cast<float4*>(&Cr[nb]) =
+                    make_float4(acc[i][4 * g] * scale, acc[i][4 * g + 1] * scale,
+                                acc[i][4 * g + 2] * scale, acc[i][4 * g + 3] * scale);
+                continue;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = 4 * g + q;
+                const int nj = GROUPED ? nb + q : n0 + tx + G::NX * j;
+                if (nj < N) {
+                    if (ksplit == 1) Cr[nj] = acc[i][j] * scale;
+                    else atomicAdd(&Cr[nj], acc[i][j] * scale);
+                }
             }
         }
     }
@@ -315,9 +332,10 @@ dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst,
 }
 
 // One row step as the matrix product above: M rows, contraction length K, N
-// outputs per row.  The forward takes 32-column tiles of 256 rows for narrow
-// outputs (2*m2 <= 32), else 64 columns by 128 rows, or by 64 rows when that
-// would leave fewer than two CTAs per SM; the inverse always 64 by 64.  If the tiles still number fewer
+// outputs per row.  Narrow forward outputs (2*m2 <= 32) take 32-column tiles of
+// 256 rows; otherwise 64 columns by 128 rows, or by 64 rows when that would
+// leave fewer than two CTAs per SM.  An inverse whose rows do not start on 16
+// bytes (W % 4 != 0) takes 64 by 64 tiles with interleaved columns.  If the tiles still number fewer
 // than two per SM, the K range is split over CTAs (chunks of at least 64) whose
 // partial sums are added into C after it is zeroed; their order of addition
 // varies from run to run.
@@ -328,14 +346,15 @@ cudaError_t launch_rows_gemm(const float* A, float* C, long long M, int K, int N
     const auto tiles = [&](int bn, int bm) {
         return ((M + bm - 1) / bm) * (long long)((N + bn - 1) / bn);
     };
-    int cfg;  // 0: <32, 4>, 1: <64, 4>, 2: <64, 2>
+    int cfg;  // 0: <32, 4>, 1: <64, 4>, 2: <64, 2>, 3: <64, 2> with interleaved columns
     long long t;
-    if (!FWD) {
-        // the inverse's K (2*m2) is short and its output (y) large: the
-        // 64-register tile at four CTAs per SM
-        cfg = 2;
+    if (!FWD && (N & 3) != 0) {
+        // rows of y that do not start on 16 bytes: interleaved columns (8 lanes
+        // store 32 contiguous bytes) at four CTAs per SM.  Measured at 421x421:
+        // 578 us, against 722 us with grouped columns
+        cfg = 3;
         t = tiles(64, RowGemm<64, 2>::BM);
-    } else if (N <= 32) {
+    } else if (FWD && N <= 32) {
         cfg = 0;
         t = tiles(32, RowGemm<32, 4>::BM);
     } else if (tiles(64, RowGemm<64, 4>::BM) >= kWant) {
@@ -358,14 +377,17 @@ cudaError_t launch_rows_gemm(const float* A, float* C, long long M, int K, int N
     }
     const unsigned grid = (unsigned)(t * ksplit);
     if (cfg == 0)
-        dft_rows_gemm_kernel<32, 4, FWD><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
-                                                              ksplit, kper);
+        dft_rows_gemm_kernel<32, 4, FWD, true><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
+                                                                    ksplit, kper);
     else if (cfg == 1)
-        dft_rows_gemm_kernel<64, 4, FWD><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
-                                                              ksplit, kper);
+        dft_rows_gemm_kernel<64, 4, FWD, true><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
+                                                                    ksplit, kper);
+    else if (cfg == 2)
+        dft_rows_gemm_kernel<64, 2, FWD, true><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
+                                                                    ksplit, kper);
     else
-        dft_rows_gemm_kernel<64, 2, FWD><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
-                                                              ksplit, kper);
+        dft_rows_gemm_kernel<64, 2, FWD, false><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
+                                                                     ksplit, kper);
     return cudaGetLastError();
 }
 
