@@ -149,13 +149,15 @@ void describe_1d(fno_plan_s* p) {
 
 cudaError_t run_forward(const fno_plan_s& p, const float* x, float2* X, float2* T, cudaStream_t s,
                         fno_launch_ctx* ctx) {
-    if (p.dims == 1) return launch_forward_1d(p, x, X, s, ctx);
+    if (p.dims == 1)
+        return p.path == 2 ? launch_forward_rows1d(p, x, X, s, ctx) : launch_forward_1d(p, x, X, s, ctx);
     return p.path == 1 ? launch_forward_fused(p, x, X, s, ctx) : launch_forward_modes(p, x, X, T, s, ctx);
 }
 
 cudaError_t run_inverse(const fno_plan_s& p, const float2* Z, float* y, float2* T, cudaStream_t s,
                         fno_launch_ctx* ctx) {
-    if (p.dims == 1) return launch_inverse_1d(p, Z, y, s, ctx);
+    if (p.dims == 1)
+        return p.path == 2 ? launch_inverse_rows1d(p, Z, y, s, ctx) : launch_inverse_1d(p, Z, y, s, ctx);
     return p.path == 1 ? launch_inverse_fused(p, Z, y, s, ctx) : launch_inverse_modes(p, Z, y, T, s, ctx);
 }
 
@@ -269,7 +271,10 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
     if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return nullptr; }
 
     int Rf = 0, Ri = 0;
-    p->path = dims == 2 && fused_supported(W, H, m1, m2, &Rf, &Ri) ? 1 : 0;
+    // path: 0 shape-generic (FFT or direct-DFT stages), 1 fused transforms,
+    // 2 the 1D layer on the long-row FFT kernels
+    if (dims == 1) p->path = rows1d_supported(W, m2) ? 2 : 0;
+    else p->path = fused_supported(W, H, m1, m2, &Rf, &Ri) ? 1 : 0;
     p->R = p->path == 1 ? Rf : H;
     p->P = H / p->R;
     p->Ri = p->path == 1 ? Ri : H;
@@ -298,8 +303,14 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
     p->ws_bytes = off;
     if (dims == 1) {
         describe_1d(p);
-        std::snprintf(p->desc, sizeof(p->desc), "1d-dft: rows(L=%d,m=%d)|%s|irows", W, m2,
-                      mix_name(p));
+        if (p->path == 2) {
+            std::snprintf(p->kernels[0].name, sizeof(p->kernels[0].name), "rows1d_fwd");
+            std::snprintf(p->kernels[2].name, sizeof(p->kernels[2].name), "rows1d_inv");
+            p->kernels[0].flops = (size_t)(fft_flops(W) * p->B * Cin / 2);
+            p->kernels[2].flops = (size_t)(fft_flops(W) * p->B * Cout / 2);
+        }
+        std::snprintf(p->desc, sizeof(p->desc), "1d-%s: rows(L=%d,m=%d)|%s|irows",
+                      p->path == 2 ? "fft" : "dft", W, m2, mix_name(p));
     } else if (p->path == 1) {
         describe_fused(p);
         std::snprintf(p->desc, sizeof(p->desc),

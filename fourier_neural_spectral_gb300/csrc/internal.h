@@ -99,6 +99,12 @@ size_t big_smem_bytes_any(int W, int R, int m2, bool fwd);
 bool big_z_staged_any(int W, int R, int m1, int m2);
 cudaError_t launch_forward_big(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s);
 cudaError_t launch_inverse_big(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s);
+// the 1D layer's row transforms on the long-row kernels (W = 512 .. 4096, m2 <= 64)
+bool rows1d_supported(int W, int m2);
+cudaError_t launch_forward_rows1d(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s,
+                                  fno_launch_ctx* ctx);
+cudaError_t launch_inverse_rows1d(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s,
+                                  fno_launch_ctx* ctx);
 
 // TMA-fed fp32 contraction (mix_tma.cu).
 cudaError_t mix_tma_init();

@@ -344,6 +344,169 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
     }
 }
 
+// ---------------------------------------------------------------- 1D rows ---
+// The 1D layer for power-of-two lengths W = L in {512, ..., 4096} with m2 = m <= 64:
+// the long-row transforms above without a column step.  Group g of CTA c takes
+// the sequences qa = 2*(c*Groups + g) and qa + 1 (a zero row when the count is
+// odd), read straight from global memory, and writes their kept bins times
+// `scale` to X[seq][k] (forward), or rebuilds their two rows from Z[seq][k]
+// (inverse).  The arithmetic is that of fwd_big_kernel / inv_big_kernel for one
+// row pair per group.
+template <int W>
+__global__ void __launch_bounds__(kBT, 2)
+fwd_rows1d_kernel(const float* __restrict__ x, float2* __restrict__ X, int S, int m2,
+                  float scale, const float2* __restrict__ tw_w) {
+    using B = BigCfg<W>;
+    constexpr int L = B::L, G = B::G, NK = B::NK;
+    __shared__ __align__(16) float2 scr[B::Groups * B::GroupScr];
+    const int g = threadIdx.x / L, t = threadIdx.x % L;
+    const int qa = 2 * (blockIdx.x * B::Groups + g);
+    const bool active = qa < S;  // uniform over the group
+    const bool has_b = qa + 1 < S;
+    griddep_wait();  // x may be the previous kernel's output
+    griddep_launch_dependents();
+    float2* Sm = scr + g * B::GroupScr;  // S[kk][n1], row stride L + G
+    float2* Zs = Sm + 16 * B::SStride;   // Zs[kk][slot]
+    const int kk2 = t / G, a = t % G;
+    float2 tw1[16], tw2[NK];
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) tw1[kk] = root<-1>(tw_w, t * kk, W);
+#pragma unroll
+    for (int j = 0; j < NK; ++j) tw2[j] = root<-1>(tw_w, 16 * a * cand_k1<L>(j), W);
+
+    if (active) {
+        const float* ra = x + (size_t)qa * W;
+        const float* rb = ra + W;
+        float2 v[16];
+#pragma unroll
+        for (int n2 = 0; n2 < 16; ++n2)
+            v[n2] = make_float2(__ldg(ra + t + L * n2), has_b ? __ldg(rb + t + L * n2) : 0.f);
+        dft<16, -1>(v);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+            Sm[kk * B::SStride + t] = kk == 0 ? v[0] : cmul(v[kk], tw1[kk]);
+    }
+    group_sync<L>(g);
+    if (active) {
+        float2 d[16];
+#pragma unroll
+        for (int b = 0; b < 16; ++b) d[b] = Sm[kk2 * B::SStride + a + G * b];
+        dft<16, -1>(d);
+        float2 r[NK];
+#pragma unroll
+        for (int j = 0; j < NK; ++j) {
+            const int k1 = cand_k1<L>(j);
+            r[j] = j < 2 * kNL ? cmul(d[k1 & 15], tw2[j]) : make_float2(0.f, 0.f);
+        }
+        reduce_scatter<NK, G>(r, a);
+#pragma unroll
+        for (int j = 0; j < NK / G; ++j) Zs[kk2 * NK + a * (NK / G) + j] = r[j];
+    }
+    group_sync<L>(g);
+    if (active) {
+        // separation of the two rows' spectra for k = 16*k1 + kk < m2
+        const float hs = 0.5f * scale;
+        for (int k = t; k < m2; k += L) {
+            const int kk = k & 15, k1 = k >> 4;
+            const float2 zk = Zs[kk * NK + k1];
+            float2 zm;  // Z[W - k]
+            if (kk == 0) {
+                zm = k1 == 0 ? Zs[0] : Zs[0 * NK + (L - k1) - L + 2 * kNL];
+            } else {
+                zm = Zs[(16 - kk) * NK + (L - 1 - k1) - L + 2 * kNL];
+            }
+            X[(size_t)qa * m2 + k] = make_float2(hs * (zk.x + zm.x), hs * (zk.y - zm.y));
+            if (has_b)
+                X[(size_t)(qa + 1) * m2 + k] = make_float2(hs * (zk.y + zm.y), -hs * (zk.x - zm.x));
+        }
+    }
+}
+
+template <int W>
+__global__ void __launch_bounds__(kBT, 2)
+inv_rows1d_kernel(const float2* __restrict__ Z, float* __restrict__ y, int S, int m2,
+                  float scale, const float2* __restrict__ tw_w) {
+    using B = BigCfg<W>;
+    constexpr int L = B::L, G = B::G, NK = B::NK;
+    constexpr int half = W / 2;
+    __shared__ __align__(16) float2 scr[B::Groups * B::GroupScr];
+    const int g = threadIdx.x / L, t = threadIdx.x % L;
+    const int qa = 2 * (blockIdx.x * B::Groups + g);
+    const bool active = qa < S;
+    const bool has_b = qa + 1 < S;
+    griddep_wait();  // Z is the previous kernel's output; y may still be read before it
+    griddep_launch_dependents();
+    float2* Sm = scr + g * B::GroupScr;
+    const int kk2 = t / G, a = t % G;
+    float2 tw1[16], tw2[NK];
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) tw1[kk] = cscale(root<1>(tw_w, t * kk, W), scale);
+#pragma unroll
+    for (int j = 0; j < NK; ++j) tw2[j] = root<1>(tw_w, 16 * a * cand_k1<L>(j), W);
+
+    if (active) {
+        const float2* Va = Z + (size_t)qa * m2;
+        const float2* Vb = Va + m2;
+        float2 e[16];
+#pragma unroll
+        for (int d = 0; d < 16; ++d) e[d] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 2 * kNL; ++j) {
+            const int k1 = cand_k1<L>(j);
+            const int k = 16 * k1 + kk2;
+            const int kr = k <= half ? k : W - k;
+            if (kr >= m2) continue;
+            const float2 va = __ldg(&Va[kr]);
+            const float2 vb = has_b ? __ldg(&Vb[kr]) : make_float2(0.f, 0.f);
+            float2 uk, um;
+            packed_bin(va, vb, kr == 0 || kr == half, &uk, &um);
+            e[k1 & 15] = cmul(k <= half ? uk : um, tw2[j]);
+        }
+        static_assert(L % 16 == 0 && 2 * kNL == 8, "candidate residues 0..3, 12..15");
+        dft16_in8<1>(e);
+#pragma unroll
+        for (int b = 0; b < 16; ++b) Sm[kk2 * B::SStride + a + G * b] = e[b];
+    }
+    group_sync<L>(g);
+    if (active) {
+        float2 v[16];
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+            v[kk] = kk == 0 ? cscale(Sm[t], scale) : cmul(Sm[kk * B::SStride + t], tw1[kk]);
+        dft<16, 1>(v);
+        float* ya = y + (size_t)qa * W;
+        float* yb = ya + W;
+#pragma unroll
+        for (int n2 = 0; n2 < 16; ++n2) {
+            ya[t + L * n2] = v[n2].x;
+            if (has_b) yb[t + L * n2] = v[n2].y;
+        }
+    }
+}
+
+template <bool FWD, int W>
+cudaError_t launch_rows1d_w(const fno_plan_s& p, const float* x, float2* X, const float2* Z,
+                            float* y, cudaStream_t s) {
+    const int S = p.B * (FWD ? p.Cin : p.Cout);
+    const int pairs = (S + 1) / 2;
+    const unsigned grid = (unsigned)((pairs + BigCfg<W>::Groups - 1) / BigCfg<W>::Groups);
+    if (FWD)
+        return launch_pdl(fwd_rows1d_kernel<W>, grid, kBT, 0, s, x, X, S, p.m2, p.scale, p.tw_w);
+    return launch_pdl(inv_rows1d_kernel<W>, grid, kBT, 0, s, Z, y, S, p.m2, p.scale, p.tw_w);
+}
+
+template <bool FWD>
+cudaError_t launch_rows1d(const fno_plan_s& p, const float* x, float2* X, const float2* Z,
+                          float* y, cudaStream_t s) {
+    switch (p.W) {
+        case 512: return launch_rows1d_w<FWD, 512>(p, x, X, Z, y, s);
+        case 1024: return launch_rows1d_w<FWD, 1024>(p, x, X, Z, y, s);
+        case 2048: return launch_rows1d_w<FWD, 2048>(p, x, X, Z, y, s);
+        case 4096: return launch_rows1d_w<FWD, 4096>(p, x, X, Z, y, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 template <int W, int R>
 cudaError_t set_attrs() {
     const int fb = (int)std::min<size_t>(big_smem_bytes<W, R, true>(64), 227 * 1024);
@@ -456,4 +619,22 @@ cudaError_t launch_forward_big(const fno_plan_s& p, const float* x, float2* X, c
 
 cudaError_t launch_inverse_big(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s) {
     return dispatch<false>(p, nullptr, nullptr, Z, y, s);
+}
+
+bool rows1d_supported(int W, int m2) {
+    return (W == 512 || W == 1024 || W == 2048 || W == 4096) && m2 <= 16 * kNL;
+}
+
+cudaError_t launch_forward_rows1d(const fno_plan_s& p, const float* x, float2* X, cudaStream_t s,
+                                  fno_launch_ctx* ctx) {
+    cudaError_t e = launch_rows1d<true>(p, x, X, nullptr, nullptr, s);
+    if (e == cudaSuccess && ctx) e = ctx->mark(s);
+    return e;
+}
+
+cudaError_t launch_inverse_rows1d(const fno_plan_s& p, const float2* Z, float* y, cudaStream_t s,
+                                  fno_launch_ctx* ctx) {
+    cudaError_t e = launch_rows1d<false>(p, nullptr, nullptr, Z, y, s);
+    if (e == cudaSuccess && ctx) e = ctx->mark(s);
+    return e;
 }

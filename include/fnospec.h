@@ -92,8 +92,8 @@ fno_status_t fno_plan_create(fno_plan_t* plan, int B, int Cin, int Cout, int H, 
  * sequence, a learned complex factor per frequency, the inverse back), with the
  * per-mode channel contraction of the TurboFNO page, section 2.2, in one
  * dimension.  Shapes: x float [B][Cin][L], w complex64 [Cin][Cout][m],
- * y float [B][Cout][L]; 2 <= L <= 4096, 1 <= m <= L/2 + 1 (any L: direct
- * DFTs).  The returned plan serves every call taking a plan (execute, the
+ * y float [B][Cout][L]; 2 <= L <= 4096, 1 <= m <= L/2 + 1 (pruned FFTs for
+ * L = 512, 1024, 2048, 4096 with m <= 64, direct DFTs otherwise).  The returned plan serves every call taking a plan (execute, the
  * three stages, the backward, the block epilogue), with H = 1, W = L, and
  * 2*m1*m2 read as m wherever a size is stated.  Errors as fno_plan_create. */
 fno_status_t fno_plan_create_1d(fno_plan_t* plan, int B, int Cin, int Cout, int L, int m,

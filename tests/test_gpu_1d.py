@@ -2,9 +2,10 @@
 
 The oracle's 1D layer and its backward are pinned on the CPU (tests/test_oracle.py:
 numpy's rfft/irfft, the circular-convolution theorem, the adjoint and weight
-identities).  Here the CUDA path -- the row transforms as direct DFTs with the
-orthonormal scale on each side, and the plan's contraction -- matches it element
-by element within the fp32 bars, on lengths that are and are not powers of two,
+identities).  Here the CUDA path -- the row transforms (pruned FFTs for
+L = 512 .. 4096 with m <= 64, direct DFTs otherwise) with the orthonormal scale
+on each side, and the plan's contraction -- matches it element by element
+within the fp32 bars, on lengths that are and are not powers of two,
 the Nyquist mode kept or not, the 32-mode contraction blocks and the
 shape-generic contraction, the longest supported sequence, and L = 2.
 """
@@ -26,6 +27,8 @@ SHAPES_1D = [
     (3, 5, 7, 4096, 9),       # longest sequence
     (1, 1, 1, 2, 2),          # L = 2: only the k = 0 and Nyquist bins
     (17, 6, 5, 256, 40),      # B > 16, 40 modes (ragged 32-mode block)
+    (3, 5, 7, 512, 40),       # FFT rows (L >= 512, m <= 64), odd sequence counts 15 / 21
+    (1, 3, 2, 2048, 64),      # FFT rows, 64 modes, 3 / 2 sequences
 ]
 
 
@@ -84,7 +87,7 @@ def test_layer_1d_tf32(cuda_lib):
 
 
 @pytest.mark.parametrize("shape", [(2, 3, 2, 16, 5), (4, 32, 32, 1024, 64), (2, 4, 6, 100, 12),
-                                   (2, 3, 3, 64, 33), (1, 1, 1, 2, 2)])
+                                   (2, 3, 3, 64, 33), (1, 1, 1, 2, 2), (3, 5, 7, 512, 40)])
 def test_backward_1d_matches_oracle(cuda_lib, shape):
     import torch
     from fourier_neural_spectral_gb300 import fnospec
