@@ -311,7 +311,14 @@ bool mix_wide_supported(int B, int Cin, int Cout, int nm) {
 cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                             bool after_own_forward, cudaStream_t s, fno_launch_ctx* ctx) {
     const int early_w = after_own_forward ? 1 : 0;
-    const int bt = wide_bt(p.B);
+    // batch tile: the power of two >= B (at most 16), halved while the grid
+    // would have fewer than two CTAs per SM (few modes and outputs); smaller
+    // tiles re-read w, which such shapes hold in L2
+    int bt = wide_bt(p.B);
+    const auto ctas = [&](int b) {
+        return (long long)((p.nm + kModes - 1) / kModes) * ((p.Cout + 7) / 8) * ((p.B + b - 1) / b);
+    };
+    while (bt > 2 && ctas(bt) < 2 * 152) bt >>= 1;
     int ic = 0, kOCB = 0;
     switch (bt) {
         case 1: ic = WideTile<1>::IC; kOCB = WideTile<1>::OCB; break;
