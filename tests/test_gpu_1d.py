@@ -29,6 +29,7 @@ SHAPES_1D = [
     (17, 6, 5, 256, 40),      # B > 16, 40 modes (ragged 32-mode block)
     (3, 5, 7, 512, 40),       # FFT rows (L >= 512, m <= 64), odd sequence counts 15 / 21
     (1, 3, 2, 2048, 64),      # FFT rows, 64 modes, 3 / 2 sequences
+    (1, 2, 3, 256, 100),      # direct DFTs with K split over CTAs both ways (2m = 200)
 ]
 
 
