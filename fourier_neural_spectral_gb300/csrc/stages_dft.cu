@@ -1,8 +1,9 @@
-// stages_dft.cu -- the transforms for grids whose H or W is not a power of two,
-// as pruned direct DFTs (the FFT kernels need power-of-two lengths).  With few
-// retained modes (the layer keeps m2 columns and 2*m1 rows) a direct sum per
-// retained bin costs W (or H) multiply-adds, which is the right order for
-// these sizes.  All four steps are the layer's definition written out:
+// stages_dft.cu -- the transforms for grids whose H or W is not a power of two
+// (and the 1D layer's rows at lengths the FFT rows do not cover), as pruned
+// direct DFTs (the FFT kernels need power-of-two lengths).  With few retained
+// modes (the layer keeps m2 columns and 2*m1 rows) a direct sum per retained
+// bin costs W (or H) multiply-adds, which is the right order for these sizes.
+// All four steps are the layer's definition written out:
 //   rows, forward:   T[q][h][k2]  = sum_w x[q][h][w] e^{-2 pi i k2 w / W},   k2 < m2
 //   cols, forward:   X[q][r][k2]  = s * sum_h T[q][h][k2] e^{-2 pi i k1(r) h / H}
 //   cols, inverse:   V[q][h][k2]  = sum_r Z[q][r][k2] e^{+2 pi i k1(r) h / H}
@@ -23,7 +24,6 @@
 namespace fno {
 namespace {
 
-
 // The row steps as real matrix products over all rows of all planes (M rows):
 //   forward  C[row][n] = sum_w x[row][w] F[w][n],  n = 2*k2 + c,  N = 2*m2:
 //            F[w][2k2] = cos(2 pi k2 w / W), F[w][2k2 + 1] = -sin(2 pi k2 w / W),
@@ -39,9 +39,9 @@ namespace {
 // stored as float4 when rows start on 16 bytes) or interleaved (columns
 // tx + NX*j, so that eight lanes store 32 contiguous bytes); per K step one
 // shared-memory float4 of A (TM = 4) and two float4 of twiddles (grouped) feed
-// TM * 8 fused multiply-adds.  The chunks are double
-// buffered: the next chunk of A is loaded into registers and its twiddles are
-// formed while the current one is multiplied.  With few output tiles the K
+// TM * 8 fused multiply-adds.  The chunks are double buffered: the next chunk
+// of A is loaded into registers and its twiddles are formed while the current
+// one is multiplied.  With few output tiles the K
 // range is split over CTAs (ksplit > 1) that add their partial sums into C,
 // which the launcher has zeroed.
 constexpr int kGT = 256;  // threads per CTA
