@@ -50,9 +50,175 @@ def read_peaks():
                 "sm_max_mhz": 2070.0}, "fallback"
 
 
-def fp32_fma_peak_tflops(sm_mhz: float, sms: int = 152) -> float:
+def fp32_fma_peak_tflops(sm_mhz: float, sms: int) -> float:
     """FP32 FMA peak: SMs x 128 lanes x 2 flops x clock."""
     return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+# dense TF32 tensor rate relative to dense bf16 (nominal 1.1 against 2.25 PFLOP/s)
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def device_sms(dev) -> int:
+    import torch
+    return int(torch.cuda.get_device_properties(dev).multi_processor_count)
+
+
+def kernel_io_bytes(name: str, cfg) -> int:
+    """The share of the layer's algorithmic bytes (x read, y written, w read:
+    the roofline's definition) that kernel `name` moves; the rest of its bytes
+    are the spectra X, Z (and T) in the plan's workspace."""
+    if name.startswith(("fwd_fused", "fwd_rows", "dft_rows", "dft1_fwd", "rows1d_fwd")):
+        return cfg.x_bytes()
+    if name.startswith(("inv_fused", "inv_rows", "dft_irows", "dft1_inv", "rows1d_inv")):
+        return cfg.y_bytes()
+    if name.startswith("mix"):
+        return cfg.w_bytes()
+    return 0
+
+
+def kernel_roofline(kinfo, ms: float, cfg, peaks: dict, sms: int, precision: str):
+    """Roofline of one kernel from its algorithmic bytes and flops: bytes are
+    its share of x + y + w (kernel_io_bytes) at the measured HBM copy peak;
+    flops (the mode contraction only; the transforms' arithmetic is secondary)
+    at the FP32 FMA peak, or at the TF32 tensor peak divided by the number of
+    TF32 products per fp32 product (3 for split TF32) on the tensor path.
+    Whichever takes longer binds; frac = that time / the measured time."""
+    hbm = float(peaks["hbm_gbs"])
+    clock = float(peaks.get("sm_max_mhz", 2070.0))
+    io = kernel_io_bytes(kinfo["name"], cfg)
+    t = ms * 1e-3
+    t_bytes = io / (hbm * 1e9)
+    flops = kinfo["flops"] if kinfo["name"].startswith("mix") else 0
+    tensor = "_tc" in kinfo["name"] or "tcgen05" in kinfo["name"]
+    if tensor:
+        split = 3 if "3xtf32" in kinfo["name"] else 1
+        cpeak = float(peaks["bf16_tflops"]) * TF32_PER_BF16 / split
+        ckind = f"tf32 tensor peak = measured bf16 x {TF32_PER_BF16:.3f} / {split}"
+    else:
+        cpeak = fp32_fma_peak_tflops(clock, sms)
+        ckind = f"fp32 FMA peak = {sms} SMs x 128 x 2 x {clock:.0f} MHz"
+    t_flops = flops / (cpeak * 1e12) if flops else 0.0
+    if t_bytes >= t_flops:
+        r = {"bound": "hbm", "achieved": io / t / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor" if tensor else "alu", "achieved": flops / t / 1e12, "peak": cpeak,
+             "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r.update({"kernel": kinfo["name"], "ms_per_launch": ms, "io_bytes_per_launch": io,
+              "workspace_bytes_per_launch": kinfo["bytes"] - io,
+              "flops_per_launch": flops, "t_bytes_us": t_bytes * 1e6,
+              "t_flops_us": t_flops * 1e6, "compute_peak_tflops": cpeak,
+              "compute_peak_kind": ckind})
+    return r
+
+
+# ---------------------------------------------------- measured DRAM traffic ---
+# profiles/dram_traffic.json holds per-launch DRAM bytes of the kernels, one
+# entry per (workload, kernel, precision), written by `--ingest-ncu` from the
+# CSV of an ncu capture with dram__bytes_read.sum and dram__bytes_write.sum.
+# Each entry records the SHA-256 of the source files its kernel is built from;
+# a lookup whose sources have changed since returns None.
+
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "dram_traffic.json")
+CSRC = os.path.join(ROOT, "fourier_neural_spectral_gb300", "csrc")
+# plan kernel name -> (regex on the demangled ncu kernel name, source files)
+_COMMON = ["common.cuh", "internal.h"]
+KERNEL_SOURCES = {
+    "fwd_fused": (r"\b(fwd_fused_kernel|fwd_big_kernel)\b",
+                  ["stages_fused.cu", "stages_big.cu", "fused_columns.cuh", "fft_reg.cuh",
+                   "tma.cuh"] + _COMMON),
+    "inv_fused": (r"\b(inv_fused_kernel|inv_big_kernel)\b",
+                  ["stages_fused.cu", "stages_big.cu", "fused_columns.cuh", "fft_reg.cuh",
+                   "tma.cuh"] + _COMMON),
+    "zero_X": (r"\bzero_kernel\b", ["stages_fused.cu"] + _COMMON),
+    "mix_wide": (r"\bmix_wide_kernel\b", ["mix_wide.cu", "tma.cuh"] + _COMMON),
+    "mix_tma": (r"\bmix_tma_kernel\b", ["mix_tma.cu", "tma.cuh"] + _COMMON),
+    "mix_tc_tf32": (r"\bmix_tc_kernel<1>", ["mix_tc.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
+    "mix_tc_3xtf32": (r"\bmix_tc_kernel<3>", ["mix_tc.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
+    "mix_tcm_3xtf32": (r"\bmix_tcm_kernel<3", ["mix_tcm.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
+    "mix_tcm_tf32": (r"\bmix_tcm_kernel<1", ["mix_tcm.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
+    "dft_rows": (r"\bdft_rows_gemm_kernel<[0-9]+, [0-9]+, true", ["stages_dft.cu"] + _COMMON),
+    "dft_irows": (r"\bdft_rows_gemm_kernel<[0-9]+, [0-9]+, false", ["stages_dft.cu"] + _COMMON),
+    "dft_cols": (r"\bdft_cols_gemm_kernel<true>", ["stages_dft.cu"] + _COMMON),
+    "dft_icols": (r"\bdft_cols_gemm_kernel<false>", ["stages_dft.cu"] + _COMMON),
+}
+
+
+def source_hashes(kernel: str) -> dict:
+    import hashlib
+    files = KERNEL_SOURCES.get(kernel, (None, sorted(os.listdir(CSRC))))[1]
+    out = {}
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            out[f] = hashlib.sha256(fh.read()).hexdigest()
+    return out
+
+
+def measured_traffic(workload: str, kernel: str, precision: str, path: str = TRAFFIC_JSON):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the
+    ingested ncu captures, or None if never captured or if its sources changed
+    since the capture."""
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in data.get("captures", []):
+        if (e["workload"], e["kernel"], e["precision"]) == (workload, kernel, precision):
+            try:
+                if source_hashes(kernel) != e["sources"]:
+                    return None
+            except OSError:
+                return None
+            return float(e["read_bytes"]) + float(e["write_bytes"])
+    return None
+
+
+def ingest_ncu(csv_path: str, workload: str, precision: str, command: str,
+               path: str = TRAFFIC_JSON) -> list:
+    """Read an ncu --csv capture (one row per launch and metric: columns
+    "Kernel Name", "Metric Name", "Metric Value") and record the median DRAM
+    read and write bytes per launch of every known kernel in it."""
+    import csv
+    import re
+    rows = {}
+    with open(csv_path, newline="") as f:
+        lines = [l for l in f if l.startswith('"')]  # skip ncu's ==PROF== lines
+    for r in csv.DictReader(lines):
+        name, metric = r.get("Kernel Name", ""), r.get("Metric Name", "")
+        if metric not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        unit = (r.get("Metric Unit") or "byte").lower()
+        scale = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9}.get(unit, 1)
+        val = float(str(r["Metric Value"]).replace(",", "")) * scale
+        for k, (rx, _) in KERNEL_SOURCES.items():
+            if re.search(rx, name):
+                rows.setdefault(k, {}).setdefault(metric, []).append(val)
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        data = {}
+    caps = [e for e in data.get("captures", [])
+            if not (e["workload"] == workload and e["precision"] == precision and e["kernel"] in rows)]
+    added = []
+    for k, m in sorted(rows.items()):
+        rd, wr = m.get("dram__bytes_read.sum", []), m.get("dram__bytes_write.sum", [])
+        if not rd or not wr:
+            continue
+        e = {"workload": workload, "kernel": k, "precision": precision,
+             "read_bytes": statistics.median(rd), "write_bytes": statistics.median(wr),
+             "launches": len(rd), "command": command, "sources": source_hashes(k)}
+        caps.append(e)
+        added.append(e)
+    data = {"about": "DRAM bytes per launch (ncu dram__bytes_read.sum / dram__bytes_write.sum, "
+                     "median over the captured launches), written by bench.py --ingest-ncu",
+            "captures": sorted(caps, key=lambda e: (e["workload"], e["kernel"], e["precision"]))}
+    with open(path, "w") as f:
+        json.dump(data, f, indent=1)
+        f.write("\n")
+    return added
 
 
 # ----------------------------------------------------------------- clocks ---
@@ -109,6 +275,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ NVTX ---
+
+class nvtx_range:
+    """An NVTX range around a region of the bench (seen by Nsight tools; a no-op
+    cost otherwise)."""
+
+    def __init__(self, name: str):
+        self.name = name
+
+    def __enter__(self):
+        import torch
+        torch.cuda.nvtx.range_push(self.name)
+
+    def __exit__(self, *exc):
+        import torch
+        torch.cuda.nvtx.range_pop()
+        return False
+
+
 # ------------------------------------------------------------ distributed ---
 
 def dist_info():
@@ -139,23 +324,6 @@ def aggregate_value(world: int, batch: int, steps: int, elapsed_ms_max: float) -
     """Whole-job samples/s: every rank runs its own replica of the workload
     (weak scaling), timed by the slowest rank."""
     return world * batch * steps / (elapsed_ms_max / 1e3)
-
-
-def measured_traffic(workload: str, kernel: str, precision: str):
-    """DRAM bytes (read + write) per launch of `kernel` on `workload`, from the
-    ncu summary table in profiles/dram_traffic.md, or None if not captured for
-    the current version of that kernel."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
-    try:
-        with open(path) as f:
-            for line in f:
-                cells = [c.strip() for c in line.strip().strip("|").split("|")]
-                if len(cells) >= 5 and cells[0] == workload and cells[1] == kernel and \
-                        cells[2] == precision:
-                    return float(cells[3]) + float(cells[4])
-    except OSError:
-        pass
-    return None
 
 
 # ---------------------------------------------------------- oracle (host) ---
@@ -289,10 +457,11 @@ def run_ours(args, cfg):
     torch.cuda.synchronize(dev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
-    t_end.record(stream)
+    with nvtx_range(f"timed steps: {cfg.name}"):
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
@@ -301,11 +470,12 @@ def run_ours(args, cfg):
     status = plan.fno_get_device_status()
     if status != fnospec.FNO_OK:
         raise RuntimeError(f"device status {status} after timed steps")
-    for i in range(nbreak):
-        plan.fno_plan_record_events(evsets[i])
-        step(args.warmup + args.steps + i)
-    plan.fno_plan_record_events(None)
-    torch.cuda.synchronize(dev)
+    with nvtx_range("per-kernel breakdown steps"):
+        for i in range(nbreak):
+            plan.fno_plan_record_events(evsets[i])
+            step(args.warmup + args.steps + i)
+        plan.fno_plan_record_events(None)
+        torch.cuda.synchronize(dev)
     if plan.fno_get_device_status() != fnospec.FNO_OK:
         raise RuntimeError("device status not clean after the breakdown steps")
 
@@ -314,23 +484,19 @@ def run_ours(args, cfg):
     ms_per_step = elapsed_ms / args.steps
     value = aggregate_value(world, cfg.B, args.steps, elapsed_ms)
 
-    # dominant kernel and its roofline
+    # dominant kernel and its roofline (the kernel with the largest mean time)
     kmean = [statistics.mean(v) for v in per_kernel]
     kdom = int(np.argmax(kmean))
     kinfo = plan.kernels[kdom]
     hbm = float(peaks["hbm_gbs"])
-    k_gbs = kinfo["bytes"] / (kmean[kdom] * 1e-3) / 1e9
-    k_flops = kinfo["flops"] / (kmean[kdom] * 1e-3) / 1e12
-    traffic = measured_traffic(cfg.name, kinfo["name"], args.precision)
-    roofline = {"kernel": kinfo["name"], "bound": "hbm", "achieved": k_gbs, "peak": hbm,
-                "unit": "GB/s", "frac": k_gbs / hbm, "traffic": traffic,
-                "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy)",
-                "bytes_per_launch": kinfo["bytes"], "ms_per_launch": kmean[kdom],
-                "achieved_tflops": k_flops}
+    sms = device_sms(dev)
+    roofline = kernel_roofline(kinfo, kmean[kdom], cfg, peaks, sms, args.precision)
+    roofline["traffic"] = measured_traffic(cfg.name, kinfo["name"], args.precision)
+    roofline["peak_kind"] = (f"{peak_kind} (hbm_gbs, STREAM-style copy)"
+                             if roofline["bound"] == "hbm" else roofline["compute_peak_kind"])
     # the layer roofline: slower of (x + y + w bytes at HBM peak) and the mode
     # contraction flops at the compute peak of the path
-    sm_mhz = (clk or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
-    fp32_peak = fp32_fma_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)))
+    fp32_peak = fp32_fma_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)), sms)
     t_hbm = step_bytes / (hbm * 1e9)
     t_gemm = cfg.gemm_flops() / (fp32_peak * 1e12)
     t_roof = max(t_hbm, t_gemm)
@@ -366,13 +532,14 @@ def run_ours(args, cfg):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        xd[0].copy_(xh, non_blocking=True)
-        plan.fno_plan_execute(xd[0], ws[0], yd[0], stream=stream)
-        yh[0].copy_(yd[0], non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    with nvtx_range("end to end, serialised"):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            xd[0].copy_(xh, non_blocking=True)
+            plan.fno_plan_execute(xd[0], ws[0], yd[0], stream=stream)
+            yh[0].copy_(yd[0], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
     serial_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     serial_value = aggregate_value(world, cfg.B, e2e_steps, serial_ms)
 
@@ -386,6 +553,8 @@ def run_ours(args, cfg):
             e.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
+    nvtx_e2e = nvtx_range("end to end, pipelined copies")
+    nvtx_e2e.__enter__()
     e0.record(stream)
     s_in.wait_event(e0)
     s_out.wait_event(e0)
@@ -407,6 +576,7 @@ def run_ours(args, cfg):
     stream.wait_event(ev_out[e2e_steps % 2])
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    nvtx_e2e.__exit__(None, None, None)
     if plan.fno_get_device_status() != fnospec.FNO_OK:
         raise RuntimeError("device status not clean after the end-to-end steps")
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
@@ -518,7 +688,7 @@ def run_ours_block(args, cfg):
     ms_per_step = elapsed_ms / args.steps
     hbm = float(peaks["hbm_gbs"])
     flops = cfg.gemm_flops() + 2 * cfg.B * cfg.Cin * cfg.Cout * cfg.H * cfg.W
-    fp32_peak = fp32_fma_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)))
+    fp32_peak = fp32_fma_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)), device_sms(dev))
     t_roof = max(step_bytes / (hbm * 1e9), flops / (fp32_peak * 1e12))
     if rank == 0:
         cfgd = config_dict(cfg, "fp32")
@@ -697,7 +867,7 @@ def run_ours_1d(args):
                 "tflops": plan.kernels[k]["flops"] / (kmean[k] * 1e-3) / 1e12}
                for k in range(nk)]
     kdom = int(np.argmax(kmean))
-    fp32_peak = fp32_fma_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)))
+    fp32_peak = fp32_fma_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)), device_sms(dev))
     gemm = 8 * B * Cin * Cout * m
     t_hbm = step_bytes / (hbm * 1e9)
     t_roof = max(t_hbm, gemm / (fp32_peak * 1e12))
@@ -761,7 +931,24 @@ def main():
                          "(any H, W in [2, 4096]); x ~ N(0,1), w ~ U[0,1)/(Cin*Cout)")
     ap.add_argument("--shape1d", default="64,64,64,4096,64",
                     help="B,Cin,Cout,L,m of the 1D layer (--pass layer1d)")
+    ap.add_argument("--ingest-ncu", metavar="CSV", default=None,
+                    help="record the DRAM bytes per launch of an ncu --csv capture of this "
+                         "workload (metrics dram__bytes_read.sum, dram__bytes_write.sum) in "
+                         "profiles/dram_traffic.json and exit (no GPU needed)")
+    ap.add_argument("--ncu-command", default="",
+                    help="the command line of that capture, stored with each entry")
     args = ap.parse_args()
+    if args.ingest_ncu:
+        if args.shape:
+            B, Cin, Cout, H, W, m1, m2 = parse_ints(args.shape, 7)
+            name = synth.LayerConfig(f"B{B}_C{Cin}x{Cout}_{H}x{W}_m{m1}x{m2}", B, Cin, Cout, H,
+                                     W, m1, m2).name
+        else:
+            name = args.config
+        for e in ingest_ncu(args.ingest_ncu, name, args.precision, args.ncu_command):
+            print(f"{e['workload']} {e['kernel']} {e['precision']}: read {e['read_bytes']:.0f} "
+                  f"write {e['write_bytes']:.0f} bytes per launch ({e['launches']} launches)")
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.pass_ == "layer1d":

@@ -72,6 +72,16 @@ fno_status_t check_device(const fno_plan_s* p) {
     return dev == p->device ? FNO_OK : FNO_ERR_INVALID_ARG;
 }
 
+// An error left pending by earlier runtime calls of this host thread (for
+// example a kernel launch the runtime rejected, such as one with an invalid
+// block size) belongs to the caller.  Entry points that enqueue work report it
+// as FNO_ERR_CUDA before enqueuing anything and leave it pending, so the caller
+// still reads it with cudaGetLastError (a sticky error of the context is
+// reported the same way).
+fno_status_t check_no_pending_error() {
+    return cudaPeekAtLastError() == cudaSuccess ? FNO_OK : FNO_ERR_CUDA;
+}
+
 // e^{+2 pi i j / N} for j in [0, N), evaluated in double and rounded once.
 std::vector<float2> twiddles(int N) {
     std::vector<float2> t(N);
@@ -176,25 +186,34 @@ fno_status_t cuda_status(cudaError_t e) {
     return FNO_ERR_CUDA;
 }
 
-std::once_flag g_init_once;
-cudaError_t g_init_err = cudaSuccess;
+// Kernel attributes (dynamic shared-memory limits) are held per device, so
+// the set-up runs once for every device a plan is created on, with that
+// device current.  g_init_done[d] is written under g_init_mu only.
+constexpr int kMaxDevices = 64;
+std::mutex g_init_mu;
+bool g_init_done[kMaxDevices] = {};
 
 fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, int m2,
                      fno_precision_t prec, fno_plan_s* parent);
 
-cudaError_t init_once() {
-    std::call_once(g_init_once, [] {
-        g_init_err = stages_generic_init();
-        if (g_init_err == cudaSuccess) g_init_err = stages_dft_init();
-        if (g_init_err == cudaSuccess) g_init_err = stages_fused_init();
-        if (g_init_err == cudaSuccess) g_init_err = stages_big_init();
-        if (g_init_err == cudaSuccess) g_init_err = mix_init();
-        if (g_init_err == cudaSuccess) g_init_err = mix_tma_init();
-        if (g_init_err == cudaSuccess) g_init_err = mix_wide_init();
-        if (g_init_err == cudaSuccess) g_init_err = block_init();
-        if (g_init_err == cudaSuccess) g_init_err = mix_tc_init();
-    });
-    return g_init_err;
+cudaError_t init_device() {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_init_mu);
+    if (g_init_done[dev]) return cudaSuccess;
+    e = stages_generic_init();
+    if (e == cudaSuccess) e = stages_dft_init();
+    if (e == cudaSuccess) e = stages_fused_init();
+    if (e == cudaSuccess) e = stages_big_init();
+    if (e == cudaSuccess) e = mix_init();
+    if (e == cudaSuccess) e = mix_tma_init();
+    if (e == cudaSuccess) e = mix_wide_init();
+    if (e == cudaSuccess) e = block_init();
+    if (e == cudaSuccess) e = mix_tc_init();
+    if (e == cudaSuccess) g_init_done[dev] = true;
+    return e;
 }
 
 // A plan and its adjoint (the backward's plan: channels swapped, contraction
@@ -203,7 +222,7 @@ fno_status_t plan_pair(fno_plan_t* out, int dims, int B, int Cin, int Cout, int 
                        int m2, fno_precision_t prec) {
     if (prec != FNO_PREC_FP32 && prec != FNO_PREC_TF32 && prec != FNO_PREC_3XTF32)
         return FNO_ERR_INVALID_ARG;
-    if (init_once() != cudaSuccess) return FNO_ERR_CUDA;
+    if (init_device() != cudaSuccess) return FNO_ERR_CUDA;
     fno_plan_s* p = plan_new(dims, B, Cin, Cout, H, W, m1, m2, prec, nullptr);
     if (!p) return FNO_ERR_CUDA;
     p->adj = plan_new(dims, B, Cout, Cin, H, W, m1, m2, FNO_PREC_FP32, p);
@@ -412,6 +431,7 @@ fno_status_t fno_plan_destroy(fno_plan_t p) {
 fno_status_t fno_plan_backward(fno_plan_t p, const float* x, const void* w, const float* gy,
                                float* gx, void* gw, void* ws, size_t ws_bytes, cudaStream_t s) {
     if (!p || !p->adj) return FNO_ERR_INVALID_ARG;
+    if (check_no_pending_error() != FNO_OK) return FNO_ERR_CUDA;
     if (!gx && !gw) return FNO_ERR_INVALID_ARG;
     fno_status_t st;
     if ((st = check_device(p)) != FNO_OK) return st;
@@ -459,6 +479,7 @@ fno_status_t fno_plan_backward(fno_plan_t p, const float* x, const void* w, cons
 fno_status_t fno_plan_execute(fno_plan_t p, const float* x, const void* w, float* y, void* ws,
                               size_t ws_bytes, cudaStream_t s) {
     if (!p) return FNO_ERR_INVALID_ARG;
+    if (check_no_pending_error() != FNO_OK) return FNO_ERR_CUDA;
     fno_status_t st;
     if ((st = check_device(p)) != FNO_OK) return st;
     if ((st = check_ptr(x, true)) != FNO_OK) return st;
@@ -509,6 +530,7 @@ fno_status_t check_block_args(const fno_plan_s* p, const float* x, const float* 
 fno_status_t fno_block_epilogue(fno_plan_t p, const float* x, const float* w_pw, const float* bias,
                                 fno_activation_t act, float* y, cudaStream_t s) {
     if (!p) return FNO_ERR_INVALID_ARG;
+    if (check_no_pending_error() != FNO_OK) return FNO_ERR_CUDA;
     fno_status_t st = check_block_args(p, x, w_pw, bias, act, y);
     if (st != FNO_OK) return st;
     return cuda_status(launch_block_epilogue(*p, x, w_pw, bias, (int)act, y, false, s));
@@ -518,6 +540,7 @@ fno_status_t fno_block_execute(fno_plan_t p, const float* x, const void* w, cons
                                const float* bias, fno_activation_t act, float* y, void* ws,
                                size_t ws_bytes, cudaStream_t s) {
     if (!p) return FNO_ERR_INVALID_ARG;
+    if (check_no_pending_error() != FNO_OK) return FNO_ERR_CUDA;
     fno_status_t st = check_block_args(p, x, w_pw, bias, act, y);
     if (st != FNO_OK) return st;
     st = fno_plan_execute(p, x, w, y, ws, ws_bytes, s);
@@ -531,6 +554,7 @@ fno_status_t fno_block_execute(fno_plan_t p, const float* x, const void* w, cons
 fno_status_t fno_forward_modes(fno_plan_t p, const float* x, void* X, void* ws, size_t ws_bytes,
                                cudaStream_t s) {
     if (!p) return FNO_ERR_INVALID_ARG;
+    if (check_no_pending_error() != FNO_OK) return FNO_ERR_CUDA;
     fno_status_t st;
     if ((st = check_device(p)) != FNO_OK) return st;
     if ((st = check_ptr(x, true)) != FNO_OK) return st;
@@ -545,6 +569,7 @@ fno_status_t fno_forward_modes(fno_plan_t p, const float* x, void* X, void* ws, 
 
 fno_status_t fno_mix_modes(fno_plan_t p, const void* X, const void* w, void* Z, cudaStream_t s) {
     if (!p) return FNO_ERR_INVALID_ARG;
+    if (check_no_pending_error() != FNO_OK) return FNO_ERR_CUDA;
     fno_status_t st;
     if ((st = check_device(p)) != FNO_OK) return st;
     if ((st = check_ptr(X, true)) != FNO_OK) return st;
@@ -559,6 +584,7 @@ fno_status_t fno_mix_modes(fno_plan_t p, const void* X, const void* w, void* Z, 
 fno_status_t fno_inverse_modes(fno_plan_t p, const void* Z, float* y, void* ws, size_t ws_bytes,
                                cudaStream_t s) {
     if (!p) return FNO_ERR_INVALID_ARG;
+    if (check_no_pending_error() != FNO_OK) return FNO_ERR_CUDA;
     fno_status_t st;
     if ((st = check_device(p)) != FNO_OK) return st;
     if ((st = check_ptr(Z, true)) != FNO_OK) return st;
@@ -621,6 +647,7 @@ extern "C" fno_status_t fno_spectral_conv2d(const float* x, const void* w, float
                                             cudaStream_t s) {
     fno_status_t st = validate_shape(B, Cin, Cout, H, W, m1, m2);
     if (st != FNO_OK) return st;
+    if (check_no_pending_error() != FNO_OK) return FNO_ERR_CUDA;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return FNO_ERR_CUDA;
     Cache& c = cache();

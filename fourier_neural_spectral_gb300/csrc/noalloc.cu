@@ -44,6 +44,12 @@ bool reachable(const void* p) {
     return true;
 }
 
+// The error word in the scratch is cleared by every call but never read back:
+// no status query covers this entry point.  Its stages must therefore stay on
+// kernels that cannot fail on the device (the shape-generic and direct-DFT
+// transforms and the per-thread contraction have no waits and no device-side
+// checks); a kernel with bounded waits would report a timeout nowhere.
+//
 // Fills both twiddle tables e^{+2 pi i j / N} (double sincospi, rounded once
 // to float) and clears the error word and the debug-flag word after it.  Nothing else in the scratch needs to
 // start at zero: X, Z and T are fully written before they are read.
@@ -75,12 +81,16 @@ extern "C" fno_status_t fno_spectral_conv2d_noalloc(const float* x, const void* 
     if (B < 1 || Cin < 1 || Cout < 1 || H < 1 || W < 1 || m1 < 1 || m2 < 1)
         return FNO_ERR_INVALID_ARG;
     if (2LL * m1 > H || (long long)m2 > W / 2 + 1) return FNO_ERR_INVALID_ARG;
-    if ((H & (H - 1)) || (W & (W - 1)) || H < 2 || W < 2 || H > 4096 || W > 4096)
-        return FNO_ERR_UNSUPPORTED;
+    // any size in [2, 4096]: powers of two take the shape-generic FFT stages,
+    // other sizes the direct-DFT stages (the same [planes][H][m2] intermediate)
+    if (H < 2 || W < 2 || H > 4096 || W > 4096) return FNO_ERR_UNSUPPORTED;
     if (!x || !w || !y) return FNO_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
          reinterpret_cast<uintptr_t>(y)) % 16)
         return FNO_ERR_INVALID_ARG;
+    // an error left pending by the caller's earlier runtime calls is reported
+    // before anything is enqueued, and left pending (as the plan entry points do)
+    if (cudaPeekAtLastError() != cudaSuccess) return FNO_ERR_CUDA;
     if (!reachable(x) || !reachable(w) || !reachable(y)) return FNO_ERR_INVALID_ARG;
 
     // Scratch layout: tw_h | tw_w | err | X | Z | T, each 256-byte aligned.

@@ -36,6 +36,11 @@
  *   - Errors detected on the host are returned immediately and nothing is
  *     enqueued.  Errors detected inside kernels set a word in device memory
  *     that fno_get_device_status reads and clears.
+ *   - A runtime error already pending on the calling host thread (one that
+ *     cudaPeekAtLastError would return, such as a launch the runtime rejected
+ *     before the call) makes every entry point that enqueues work return
+ *     FNO_ERR_CUDA before enqueuing anything.  The error is left pending: it
+ *     belongs to the caller, who reads and clears it with cudaGetLastError.
  */
 #ifndef FNOSPEC_H_
 #define FNOSPEC_H_
@@ -72,7 +77,12 @@ typedef enum {
 
 typedef struct fno_plan_s* fno_plan_t;
 
-/* Human-readable name of a status code (static storage, never NULL). */
+/* Human-readable name of a status code (static storage, never NULL).
+ * The codes separate the failure classes the FFT operator-optimisation page
+ * (lpnh.cn/news/2688017) tells apart when it debugs such an operator: section
+ * 6.1 and the symptom table that closes section 6.2 (wrong arguments and
+ * out-of-range layouts, unsupported sizes, runtime failures), plus the
+ * device-side timeouts of this library's bounded waits. */
 const char* fno_status_string(fno_status_t status);
 
 /* Create a plan for one shape on the CURRENT device.  Host-side call: validates
@@ -99,7 +109,11 @@ fno_status_t fno_plan_create(fno_plan_t* plan, int B, int Cin, int Cout, int H, 
 fno_status_t fno_plan_create_1d(fno_plan_t* plan, int B, int Cin, int Cout, int L, int m,
                                 fno_precision_t prec);
 
-/* Bytes of device workspace fno_plan_execute needs (may be 0). */
+/* Bytes of device workspace fno_plan_execute needs (may be 0): the retained
+ * spectra X and Z (and, on the shape-generic path, the row/column
+ * intermediate).  Query once per plan and allocate once, as the FFT
+ * operator-optimisation page, section 5.3, does with cuFFT's workspace size
+ * query.  *bytes is written on FNO_OK; FNO_ERR_INVALID_ARG for NULL arguments. */
 fno_status_t fno_plan_workspace_size(fno_plan_t plan, size_t* bytes);
 
 /* Number of kernel launches one fno_plan_execute enqueues. */
@@ -122,7 +136,11 @@ fno_status_t fno_plan_kernel_info(fno_plan_t plan, int index, char* name, size_t
  * execute of the same plan. */
 fno_status_t fno_plan_record_events(fno_plan_t plan, cudaEvent_t* events, int count);
 
-/* Run the whole layer y = irfft2(mix(rfft2(x), w)) on stream s.
+/* Run the whole layer y = irfft2(mix(rfft2(x), w)) on stream s: the fused
+ * FFT -> per-mode contraction -> inverse FFT operator of the TurboFNO page,
+ * sections 1 and 2.2 (low modes kept, every other bin zero, the complex
+ * product per retained mode), with the orthonormal scale of its section 3.1,
+ * as the stages a1-a5 in this header's preamble define it.
  * x: float [B][Cin][H][W]; w: complex64 [Cin][Cout][2*m1][m2];
  * y: float [B][Cout][H][W]; workspace: device buffer of at least
  * fno_plan_workspace_size bytes (NULL allowed when that size is 0), owned by the
@@ -177,15 +195,21 @@ fno_status_t fno_plan_backward(fno_plan_t plan, const float* x, const void* w, c
                                float* gx, void* gw, void* workspace, size_t workspace_bytes,
                                cudaStream_t s);
 
-/* Release the plan's tables and error word.  Safe on NULL.  The caller must make
- * sure no work that uses the plan is still running. */
+/* Release the plan's tables and error word (the counterpart of the plan cache
+ * and reuse of the FFT operator-optimisation page, section 5.3: a plan lives as
+ * long as its shape is in use).  Safe on NULL; always FNO_OK.  The caller must
+ * make sure no work that uses the plan is still running. */
 fno_status_t fno_plan_destroy(fno_plan_t plan);
 
-/* One-shot form of fno_plan_execute with FNO_PREC_FP32.  Keeps an internal cache
- * of plans keyed by (device, shape) and of workspaces keyed by (device, shape,
- * stream); the first call for a key allocates (cudaMalloc), so make it before
- * any stream capture.  Calls with the same key must not overlap on the GPU
- * (they share the workspace). */
+/* One-shot form of fno_plan_execute with FNO_PREC_FP32: the layer of the
+ * TurboFNO page (sections 1, 2.2 and 3.1) behind the plan and workspace cache
+ * that the FFT operator-optimisation page, section 5.3, prescribes (plans and
+ * workspaces keyed by shape, created on the first request and reused).  Keeps
+ * an internal cache of plans keyed by (device, shape) and of workspaces keyed by
+ * (device, shape, stream); the first call for a key allocates (cudaMalloc), so
+ * make it before any stream capture.  Calls with the same key must not overlap
+ * on the GPU (they share the workspace).  Errors: as fno_plan_create and
+ * fno_plan_execute. */
 fno_status_t fno_spectral_conv2d(const float* x, const void* w, float* y, int B, int Cin,
                                  int Cout, int H, int W, int m1, int m2, cudaStream_t s);
 
@@ -212,10 +236,13 @@ fno_status_t fno_mix_modes(fno_plan_t plan, const void* X, const void* w, void* 
 fno_status_t fno_inverse_modes(fno_plan_t plan, const void* Z, float* y, void* workspace,
                                size_t workspace_bytes, cudaStream_t s);
 
-/* The whole layer (same arguments and result as fno_spectral_conv2d, fp32
- * path) for callers that cannot allocate device memory: this entry point calls
- * no cudaMalloc, cudaFree or other allocating routine.  The pages have no
- * counterpart; it exists for hosts that own every allocation themselves.
+/* The whole layer (same arguments, shapes and result as fno_spectral_conv2d,
+ * fp32 path) for callers that cannot allocate device memory: this entry point
+ * calls no cudaMalloc, cudaFree or other allocating routine.  The pages have no
+ * counterpart; it exists for hosts that own every allocation themselves.  It
+ * runs the shape-generic transform kernels (FFTs for powers of two, direct DFTs
+ * otherwise) and the per-thread fp32 contraction, none of which waits on the
+ * device, so there is no device status to query for it.
  * Its scratch (twiddle tables, error word, the spectra X and Z, the row/column
  * intermediate) lives in one static device array of 16 MiB that every GPU
  * loading the library holds until exit; shapes whose scratch does not fit
@@ -232,7 +259,11 @@ fno_status_t fno_spectral_conv2d_noalloc(const float* x, const void* w, float* y
                                          cudaStream_t s);
 
 /* Synchronise stream s, read and clear the plan's device error word.  Returns
- * FNO_OK, FNO_ERR_TIMEOUT or FNO_ERR_DEVICE (or FNO_ERR_CUDA if the copy fails). */
+ * FNO_OK, FNO_ERR_TIMEOUT or FNO_ERR_DEVICE (or FNO_ERR_CUDA if the copy fails).
+ * This is the stage-by-stage fault check of the FFT operator-optimisation page,
+ * sections 6.1 and 6.4 (find which step went wrong before looking at numbers),
+ * for faults that only the kernels can see: a bounded wait that gave up.  The
+ * plan's error word is shared with its backward; the caller owns s. */
 fno_status_t fno_get_device_status(fno_plan_t plan, cudaStream_t s);
 
 /* Test hook for the failure path: with enable != 0, every bounded wait inside

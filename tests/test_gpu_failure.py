@@ -106,3 +106,96 @@ def test_force_timeout_rejects_null_plan(cuda_lib):
     from fourier_neural_spectral_gb300 import fnospec
     lib = fnospec.load_library()
     assert lib.fno_plan_debug_force_timeout(None, 1) == fnospec.FNO_ERR_INVALID_ARG
+
+
+def _cudart():
+    """The CUDA runtime instance libfnospec is linked against (the one already
+    loaded in this process under its soname), for the pending-error cases."""
+    import ctypes
+    import os
+    from fourier_neural_spectral_gb300 import fnospec
+    fnospec.load_library()
+    try:
+        rt = ctypes.CDLL("libcudart.so.13", mode=os.RTLD_NOLOAD | ctypes.RTLD_GLOBAL)
+    except OSError:
+        rt = ctypes.CDLL("libcudart.so.13")
+    for f in ("cudaGetLastError", "cudaPeekAtLastError", "cudaSetDevice", "cudaGetDeviceCount"):
+        getattr(rt, f).restype = ctypes.c_int
+    return rt
+
+
+def test_pending_runtime_error_is_reported_before_any_work(cuda_lib):
+    """A stream whose host thread holds an unread runtime error: made on the
+    host only (cudaSetDevice with an ordinal past the device count, which the
+    runtime rejects without touching a GPU).  Every entry point that enqueues
+    work returns FNO_ERR_CUDA without enqueuing anything and leaves the error
+    pending for its owner; once the caller has read it, the next call is
+    correct."""
+    import ctypes
+    import torch
+    from fourier_neural_spectral_gb300 import fnospec
+    lib = fnospec.load_library()
+    rt = _cudart()
+    shape = B, Cin, Cout, H, W, m1, m2 = 2, 32, 32, 64, 64, 16, 16
+    rng = np.random.default_rng(99)
+    x, w = rand_layer_inputs(rng, B, Cin, Cout, H, W, m1, m2)
+    plan = fnospec.Plan(*shape, "fp32")
+    xt, wt = to_dev(x), to_dev(w)
+    y = torch.full((B, Cout, H, W), float("nan"), dtype=torch.float32, device="cuda")
+    ws_ptr, ws_n = plan._ws(None)
+    s = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    assert rt.cudaGetLastError() == 0
+
+    n = ctypes.c_int()
+    assert rt.cudaGetDeviceCount(ctypes.byref(n)) == 0
+    bad = rt.cudaSetDevice(n.value + 7)
+    assert bad != 0 and rt.cudaPeekAtLastError() == bad
+    calls = [
+        lambda: lib.fno_plan_execute(plan.handle, xt.data_ptr(), wt.data_ptr(), y.data_ptr(),
+                                     ws_ptr, ws_n, s),
+        lambda: lib.fno_spectral_conv2d(xt.data_ptr(), wt.data_ptr(), y.data_ptr(), *shape, s),
+        lambda: lib.fno_spectral_conv2d_noalloc(xt.data_ptr(), wt.data_ptr(), y.data_ptr(),
+                                                *shape, s),
+        lambda: lib.fno_forward_modes(plan.handle, xt.data_ptr(), y.data_ptr(), ws_ptr, ws_n, s),
+    ]
+    for call in calls:
+        assert call() == fnospec.FNO_ERR_CUDA
+        assert rt.cudaPeekAtLastError() == bad  # still the caller's, unread
+    assert rt.cudaGetLastError() == bad        # the caller reads (and clears) it
+    assert rt.cudaPeekAtLastError() == 0
+    torch.cuda.synchronize()
+    assert bool(torch.isnan(y).all())          # nothing was enqueued
+
+    assert lib.fno_plan_execute(plan.handle, xt.data_ptr(), wt.data_ptr(), y.data_ptr(), ws_ptr,
+                                ws_n, s) == fnospec.FNO_OK
+    torch.cuda.synchronize()
+    assert plan.fno_get_device_status() == fnospec.FNO_OK
+    assert_fp32_close(y.cpu().numpy(), oracle.spectral_conv2d(x, f32pairs_to_cplx(w), m1, m2),
+                      "after the pending error was read")
+
+
+def test_plans_on_every_device_get_their_kernel_limits(cuda_lib):
+    """Kernel attributes (the fused kernels' dynamic shared-memory limits) are
+    set per device: a plan created on each visible device, after switching the
+    current device back and forth, runs the fused 128x128 kernels (over 48 KB of
+    shared memory) correctly."""
+    import torch
+    from fourier_neural_spectral_gb300 import fnospec
+    shape = B, Cin, Cout, H, W, m1, m2 = 2, 16, 16, 128, 128, 32, 32
+    rng = np.random.default_rng(5)
+    x, w = rand_layer_inputs(rng, B, Cin, Cout, H, W, m1, m2)
+    ref = oracle.spectral_conv2d(x, f32pairs_to_cplx(w), m1, m2)
+    n = torch.cuda.device_count()
+    for rep in range(2):
+        for d in list(range(n)) + [0]:
+            with torch.cuda.device(d):
+                plan = fnospec.Plan(*shape, "fp32")
+                assert "fused" in plan.description
+                xt = torch.from_numpy(x).to(f"cuda:{d}")
+                wt = torch.from_numpy(w).to(f"cuda:{d}")
+                y = torch.empty((B, Cout, H, W), dtype=torch.float32, device=f"cuda:{d}")
+                plan.fno_plan_execute(xt, wt, y)
+                torch.cuda.synchronize(d)
+                assert plan.fno_get_device_status() == fnospec.FNO_OK
+                assert_fp32_close(y.cpu().numpy(), ref, f"device {d}")

@@ -30,9 +30,11 @@ def test_layer_matches_oracle_elementwise(cuda_lib, name):
     print(f"{name}: {plan.description} rel-L2 {rel:.2e} max-abs {mx:.2e}")
 
 
-def test_2048_grid_sampled_and_forward_stage(cuda_lib):
-    """Full 2048x2048 workload: the forward stage is compared in full, the layer
-    output at 4096 sampled points (corners, edges and random interior)."""
+def test_2048_grid_full_layer_and_forward_stage(cuda_lib):
+    """Full 2048x2048 workload: the forward stage and the whole layer output are
+    compared with the oracle element by element over the full tensors (the
+    oracle's planes run on host threads), plus corner and edge points of y
+    against the oracle's pointwise inverse."""
     import torch
     from fourier_neural_spectral_gb300 import fnospec
     cfg = synth.CONFIGS["B2_C32_2048x2048_m64"]
@@ -48,21 +50,31 @@ def test_2048_grid_sampled_and_forward_stage(cuda_lib):
     X_ref = oracle.forward_modes_parallel(x, cfg.m1, cfg.m2)
     assert_fp32_close(f32pairs_to_cplx(Xt.cpu().numpy()), X_ref, "forward stage")
     Z_ref = oracle.mix_modes(X_ref, f32pairs_to_cplx(w))
-    rng = np.random.default_rng(5)
-    n = 4096
-    idx = np.stack([rng.integers(0, cfg.B, n), rng.integers(0, cfg.Cout, n),
-                    rng.integers(0, cfg.H, n), rng.integers(0, cfg.W, n)], axis=1)
-    idx[:8, 2:] = [[0, 0], [0, cfg.W - 1], [cfg.H - 1, 0], [cfg.H - 1, cfg.W - 1],
-                   [cfg.H // 2, cfg.W // 2], [1, 1], [cfg.H - 2, 3], [7, cfg.W - 5]]
-    ref = oracle.inverse_modes_at(Z_ref, cfg.H, cfg.W, idx)
-    got = yt[tuple(torch.from_numpy(idx).long().cuda().T)].cpu().numpy()
-    rel, mx = errors(got, ref)
-    # sampled points: same bounds, measured over the sample
+    del X_ref
+    y = yt.cpu().numpy()
+    # whole output: the same two bounds as every fp32 case, accumulated over
+    # the batch rows so that only one row's double copies are alive at a time
+    num = den = 0.0
+    dmax = rmax = 0.0
+    for b in range(cfg.B):
+        ref_b = oracle.inverse_modes_parallel(Z_ref[b:b + 1], cfg.H, cfg.W)[0]
+        d = y[b].astype(np.float64) - ref_b
+        num += float(np.vdot(d, d).real)
+        den += float(np.vdot(ref_b, ref_b).real)
+        dmax = max(dmax, float(np.abs(d).max()))
+        rmax = max(rmax, float(np.abs(ref_b).max()))
+        del d, ref_b
+    rel, mx = (num / den) ** 0.5, dmax / rmax
+    print(f"2048x2048 layer: rel-L2 {rel:.2e} max-abs {mx:.2e}")
     assert rel <= 1e-5 and mx <= 1e-4, (rel, mx)
-    # a property that holds at any size: total energy is bounded by the input's
-    # (the per-mode weights have |w| < sqrt(2)/(Cin*Cout), so |Z| <= |X| * sqrt(2)/Cout)
-    y = yt.double()
-    assert torch.isfinite(y).all()
+    # corners and edges once more through the oracle's pointwise inverse (an
+    # independent evaluation of the same sums)
+    idx = np.array([[0, 0, 0, 0], [0, 1, 0, cfg.W - 1], [1, 2, cfg.H - 1, 0],
+                    [1, cfg.Cout - 1, cfg.H - 1, cfg.W - 1], [0, 5, cfg.H // 2, cfg.W // 2],
+                    [1, 7, 1, 1], [0, 9, cfg.H - 2, 3], [1, 11, 7, cfg.W - 5]])
+    ref = oracle.inverse_modes_at(Z_ref, cfg.H, cfg.W, idx)
+    got = y[tuple(idx.T)]
+    assert np.abs(got - ref).max() <= 1e-4 * rmax
 
 
 @pytest.mark.parametrize("name", SMALL)

@@ -479,3 +479,61 @@ def test_block_1d_special_cases():
                 v = bias[o] + sum(wpw[o, i] * x[b, i, n] for i in range(Cin))
                 want = 0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0)))
                 assert abs(out[b, o, n] - want) < 1e-12
+
+
+# ------------------------------------------- threaded wrappers (full-size) ---
+# forward_modes_parallel / inverse_modes_parallel re-slice the planes over host
+# threads to build the references of the large parity cases.  The arithmetic
+# per plane is the serial oracle's, so the results must be bit-identical to it;
+# they are also compared with numpy's pocketfft directly, so that a plane-order
+# or reshape mistake (planes swapped, batch and channel transposed, a plane
+# skipped by the striding) fails even where the serial path would too.
+
+PARALLEL_SHAPES = [
+    # B, C, H, W, m1, m2, threads
+    (2, 3, 8, 16, 2, 5, 4),      # 6 planes over 4 threads (uneven stride)
+    (3, 2, 16, 8, 4, 3, 16),     # more threads than planes
+    (1, 5, 12, 10, 3, 6, 2),     # sizes that are not powers of two, Nyquist column kept
+    (4, 1, 4, 32, 2, 17, 1),     # one thread, full half spectrum along W
+    (2, 4, 16, 16, 8, 9, 3),     # 2*m1 = H, full modes
+]
+
+
+@pytest.mark.parametrize("B,C,H,W,m1,m2,threads", PARALLEL_SHAPES)
+def test_forward_modes_parallel_equals_serial(B, C, H, W, m1, m2, threads):
+    x = RNG.standard_normal((B, C, H, W))
+    Xp = oracle.forward_modes_parallel(x, m1, m2, threads=threads)
+    Xs = oracle.forward_modes(x, m1, m2)
+    assert Xp.shape == (B, C, 2 * m1, m2)
+    assert np.array_equal(Xp, Xs)
+    F = np.fft.rfft2(x, norm="ortho")[:, :, kept_rows(H, m1), :m2]
+    assert np.abs(Xp - F).max() < 1e-13
+
+
+@pytest.mark.parametrize("B,C,H,W,m1,m2,threads", PARALLEL_SHAPES)
+def test_inverse_modes_parallel_equals_serial(B, C, H, W, m1, m2, threads):
+    Z = RNG.standard_normal((B, C, 2 * m1, m2)) + 1j * RNG.standard_normal((B, C, 2 * m1, m2))
+    yp = oracle.inverse_modes_parallel(Z, H, W, threads=threads)
+    ys = oracle.inverse_modes(Z, H, W)
+    assert yp.shape == (B, C, H, W)
+    assert np.array_equal(yp, ys)
+    full = np.zeros((B, C, H, W // 2 + 1), complex)
+    full[:, :, kept_rows(H, m1), :m2] = Z
+    assert np.abs(yp - np.fft.irfft2(full, s=(H, W), norm="ortho")).max() < 1e-13
+
+
+def test_parallel_wrappers_keep_plane_identity():
+    """Each plane carries a distinct constant: the DC bin of plane (b, c) must
+    come back at (b, c), and the inverse of a DC-only spectrum is that constant
+    over the plane (orthonormal scale: DC = sqrt(HW) * value)."""
+    B, C, H, W = 3, 4, 8, 8
+    vals = np.arange(1, B * C + 1, dtype=np.float64).reshape(B, C)
+    x = np.broadcast_to(vals[:, :, None, None], (B, C, H, W)).copy()
+    X = oracle.forward_modes_parallel(x, 2, 2, threads=5)
+    assert np.abs(X[:, :, 0, 0] - vals * np.sqrt(H * W)).max() < 1e-12
+    X[:, :, 0, 0] = 0
+    assert np.abs(X).max() < 1e-12
+    Z = np.zeros((B, C, 4, 2), complex)
+    Z[:, :, 0, 0] = vals * np.sqrt(H * W)
+    y = oracle.inverse_modes_parallel(Z, H, W, threads=7)
+    assert np.abs(y - x).max() < 1e-12
