@@ -113,6 +113,7 @@ void set_kernel(fno_plan_s* p, int k, const char* name, size_t bytes, size_t flo
 
 const char* mix_name(const fno_plan_s* p) {
     if (p->mix_path == 2) return p->tc_split == 3 ? "mix_tc_3xtf32" : "mix_tc_tf32";
+    if (p->mix_path == 5) return p->tc_split == 3 ? "mix_tcm_3xtf32" : "mix_tcm_tf32";
     if (p->mix_path == 3) return p->adjoint ? "mix_wide_adj" : "mix_wide";
     if (p->mix_path == 4) return "mix_adj_fma";
     return p->mix_path == 1 ? "mix_tma" : "mix_fma";
@@ -175,6 +176,7 @@ cudaError_t run_inverse(const fno_plan_s& p, const float2* Z, float* y, float2* 
 cudaError_t run_mix(const fno_plan_s& p, const float2* X, const float2* w, float2* Z, cudaStream_t s,
                     fno_launch_ctx* ctx, bool after_own_forward) {
     if (p.mix_path == 2) return launch_mix_tc(p, X, w, Z, p.tc_split, s, ctx);
+    if (p.mix_path == 5) return launch_mix_tcm(p, X, w, Z, p.tc_split, after_own_forward, s, ctx);
     if (p.mix_path == 3) return launch_mix_wide(p, X, w, Z, after_own_forward, s, ctx);
     if (p.mix_path == 4) return launch_mix_adjoint_fma(p, X, w, Z, s, ctx);
     return p.mix_path == 1 ? launch_mix_tma(p, X, w, Z, s, ctx) : launch_mix_modes(p, X, w, Z, s, ctx);
@@ -212,6 +214,7 @@ cudaError_t init_device() {
     if (e == cudaSuccess) e = mix_wide_init();
     if (e == cudaSuccess) e = block_init();
     if (e == cudaSuccess) e = mix_tc_init();
+    if (e == cudaSuccess) e = mix_tcm_init();
     if (e == cudaSuccess) g_init_done[dev] = true;
     return e;
 }
@@ -287,7 +290,11 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
     p->nm = dims == 1 ? m2 : 2 * m1 * m2;
     p->prec = prec;
     p->scale = (float)(1.0 / std::sqrt((double)H * (double)W));
-    if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return nullptr; }
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+        delete p;
+        return nullptr;
+    }
 
     int Rf = 0, Ri = 0;
     // path: 0 shape-generic (FFT or direct-DFT stages), 1 fused transforms,
@@ -305,9 +312,14 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
     if (mix_wide_supported(B, Cin, Cout, p->nm)) p->mix_path = 3;
     p->tc_split = prec == FNO_PREC_3XTF32 ? 3 : 1;
     // tensor cores for the contraction only where it is a real dense product
-    if (prec != FNO_PREC_FP32 && Cin >= 32 && Cout >= 32 &&
-        mix_tc_supported(B, Cin, Cout, p->nm, p->tc_split))
-        p->mix_path = 2;
+    // (Cin, Cout >= 32): the weight-in-TMEM kernel for batches up to 16, the
+    // shared-memory-operand kernel for larger batches
+    if (prec != FNO_PREC_FP32 && Cin >= 32 && Cout >= 32) {
+        if (mix_tcm_supported(B, Cin, Cout, p->nm))
+            p->mix_path = 5;
+        else if (mix_tc_supported(B, Cin, Cout, p->nm, p->tc_split))
+            p->mix_path = 2;
+    }
     if (p->adjoint) p->mix_path = mix_wide_supported(B, Cin, Cout, p->nm) ? 3 : 4;
 
     // workspace: X | Z | T (T only on the shape-generic path)

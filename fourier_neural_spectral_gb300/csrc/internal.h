@@ -58,6 +58,7 @@ struct fno_plan_s {
     int nm;                 // retained modes per plane: 2*m1*m2 (m2 for the 1D layer)
     fno_precision_t prec;
     int device;
+    int sms;                // multiprocessors of the device (persistent grids)
     float scale;            // 1/sqrt(H*W), rounded once from double
     float2* tw_h;           // e^{+2 pi i j / H}, j in [0, H)
     float2* tw_w;           // e^{+2 pi i j / W}, j in [0, W)
@@ -66,12 +67,13 @@ struct fno_plan_s {
     size_t off_X, off_Z, off_T, ws_bytes;
     int path;               // 0: shape-generic kernels, 1: fused transform kernels
     int mix_path;           // 0: mix_fma, 1: mix_tma, 2: mix_tc (tcgen05), 3: mix_wide,
-                            // 4: mix_adj_fma (adjoint plans only)
+                            // 4: mix_adj_fma (adjoint plans only), 5: mix_tcm (tcgen05,
+                            // weights in tensor memory)
     bool adjoint;           // contraction with w conjugated and transposed (backward's
                             // plan: Cin, Cout are w's Cout, Cin)
     fno_plan_s* adj;        // the backward's plan (channels swapped), owned
     bool shares_tables;     // tw_h, tw_w and err belong to the parent plan
-    int tc_split;           // mix_tc: 1 (TF32) or 3 (split TF32, hi*hi + hi*lo + lo*hi)
+    int tc_split;           // mix_tc, mix_tcm: 1 (TF32) or 3 (split TF32, hi*hi + hi*lo + lo*hi)
     int R, P;               // fused path, forward: column length per CTA and H / R
     int Ri, Pi;             // fused path, inverse: the same
     int launches;           // kernel launches per execute
@@ -141,6 +143,14 @@ cudaError_t mix_tc_init();
 bool mix_tc_supported(int B, int Cin, int Cout, int nm, int split);
 cudaError_t launch_mix_tc(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                           int split, cudaStream_t s, fno_launch_ctx* ctx);
+
+// tcgen05 contraction with the weight operand in tensor memory (mix_tcm.cu):
+// 8 modes x 64 output channels per CTA, batch up to 16.
+cudaError_t mix_tcm_init();
+bool mix_tcm_supported(int B, int Cin, int Cout, int nm);
+cudaError_t launch_mix_tcm(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
+                           int split, bool after_own_forward, cudaStream_t s,
+                           fno_launch_ctx* ctx);
 
 // Direct-DFT transforms for H or W not a power of two (stages_dft.cu); the
 // shape-generic launchers below route such shapes there.

@@ -25,7 +25,8 @@ CASES = [
     # (B, Cin, Cout, H, W, m1, m2), precision, kernel the waits belong to
     ((2, 64, 64, 128, 128, 32, 32), "fp32", "inv_fused"),    # mix_wide + staged Z
     ((1, 8, 8, 512, 512, 16, 16), "fp32", "fwd_fused"),     # long rows: staged pairs, staged Z
-    ((2, 32, 32, 64, 64, 16, 16), "tf32", "mix_tc"),        # tcgen05 contraction
+    ((2, 32, 32, 64, 64, 16, 16), "tf32", "mix_tcm"),       # tcgen05, weights in TMEM
+    ((32, 32, 32, 16, 16, 4, 4), "tf32", "mix_tc_"),        # tcgen05, operands in smem
 ]
 
 

@@ -16,12 +16,15 @@ SPLIT_REL_L2 = 1e-5
 SPLIT_MAX_ABS = FP32_MAX_ABS
 
 MIX_SHAPES = [
-    # B, Cin, Cout, m1, m2
-    (1, 32, 32, 1, 2),      # one CTA: 4 modes, padded batch and channel block
-    (16, 64, 64, 4, 4),     # the 128x128 workload's channel/batch shape
-    (4, 128, 128, 2, 4),    # two channel blocks, batch padded 4 -> 8
-    (3, 40, 100, 3, 2),     # ragged Cin (last chunk partial) and Cout (partial block)
-    (32, 64, 64, 1, 2),     # largest batch handled
+    # B, Cin, Cout, m1, m2, kernel: the weight-in-TMEM kernel (mix_tcm) serves
+    # batches up to 16, the shared-memory-operand kernel (mix_tc) larger ones
+    (1, 32, 32, 1, 2, "mix_tcm"),      # one CTA, 4 of its 8 modes, batch padded 1 -> 8
+    (16, 64, 64, 4, 4, "mix_tcm"),     # the 128x128 workload's channel/batch shape
+    (4, 128, 128, 2, 4, "mix_tcm"),    # two channel blocks, batch padded 4 -> 8
+    (3, 40, 100, 3, 2, "mix_tcm"),     # ragged Cin (last chunk partial) and Cout (partial block)
+    (9, 48, 72, 3, 3, "mix_tcm"),      # batch padded 9 -> 16, 18 modes (partial mode block)
+    (16, 64, 64, 32, 32, "mix_tcm"),   # the whole 128x128 contraction (2048 modes)
+    (32, 64, 64, 1, 2, "mix_tc"),      # largest batch handled (shared-memory operands)
 ]
 
 
@@ -47,15 +50,15 @@ def mix_case(B, Cin, Cout, m1, m2, precision):
 
 @pytest.mark.parametrize("shape", MIX_SHAPES)
 def test_tc_mix_stage_tf32(cuda_lib, shape):
-    (rel, mx), plan = mix_case(*shape, "tf32")
-    assert "mix_tc_tf32" in plan.description, plan.description
+    (rel, mx), plan = mix_case(*shape[:5], "tf32")
+    assert f"{shape[5]}_tf32" in plan.description, plan.description
     assert rel <= TF32_REL_L2, rel
 
 
 @pytest.mark.parametrize("shape", MIX_SHAPES)
 def test_tc_mix_stage_split_tf32(cuda_lib, shape):
-    (rel, mx), plan = mix_case(*shape, "3xtf32")
-    assert "mix_tc_3xtf32" in plan.description, plan.description
+    (rel, mx), plan = mix_case(*shape[:5], "3xtf32")
+    assert f"{shape[5]}_3xtf32" in plan.description, plan.description
     assert rel <= SPLIT_REL_L2 and mx <= SPLIT_MAX_ABS, (rel, mx)
 
 
