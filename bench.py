@@ -74,6 +74,8 @@ def kernel_io_bytes(name: str, cfg) -> int:
         return cfg.y_bytes()
     if name.startswith("mix"):
         return cfg.w_bytes()
+    if name.startswith("layer_persistent"):  # the whole layer in one launch
+        return cfg.x_bytes() + cfg.y_bytes() + cfg.w_bytes()
     return 0
 
 
@@ -89,7 +91,7 @@ def kernel_roofline(kinfo, ms: float, cfg, peaks: dict, sms: int, precision: str
     io = kernel_io_bytes(kinfo["name"], cfg)
     t = ms * 1e-3
     t_bytes = io / (hbm * 1e9)
-    flops = kinfo["flops"] if kinfo["name"].startswith("mix") else 0
+    flops = kinfo["flops"] if kinfo["name"].startswith(("mix", "layer_persistent")) else 0
     tensor = "_tc" in kinfo["name"] or "tcgen05" in kinfo["name"]
     if tensor:
         split = 3 if "3xtf32" in kinfo["name"] else 1
@@ -127,10 +129,10 @@ _COMMON = ["common.cuh", "internal.h"]
 KERNEL_SOURCES = {
     "fwd_fused": (r"\b(fwd_fused_kernel|fwd_big_kernel)\b",
                   ["stages_fused.cu", "stages_big.cu", "fused_columns.cuh", "fft_reg.cuh",
-                   "tma.cuh"] + _COMMON),
+                   "tma.cuh", "fused_rows.cuh"] + _COMMON),
     "inv_fused": (r"\b(inv_fused_kernel|inv_big_kernel)\b",
                   ["stages_fused.cu", "stages_big.cu", "fused_columns.cuh", "fft_reg.cuh",
-                   "tma.cuh"] + _COMMON),
+                   "tma.cuh", "fused_rows.cuh"] + _COMMON),
     "zero_X": (r"\bzero_kernel\b", ["stages_fused.cu"] + _COMMON),
     "mix_wide": (r"\bmix_wide_kernel\b", ["mix_wide.cu", "tma.cuh"] + _COMMON),
     "mix_tma": (r"\bmix_tma_kernel\b", ["mix_tma.cu", "tma.cuh"] + _COMMON),
@@ -138,6 +140,9 @@ KERNEL_SOURCES = {
     "mix_tc_3xtf32": (r"\bmix_tc_kernel<3>", ["mix_tc.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
     "mix_tcm_3xtf32": (r"\bmix_tcm_kernel<3", ["mix_tcm.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
     "mix_tcm_tf32": (r"\bmix_tcm_kernel<1", ["mix_tcm.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
+    "layer_persistent": (r"\blayer_persistent_kernel\b",
+                         ["layer_persistent.cu", "fused_rows.cuh", "fused_columns.cuh",
+                          "fft_reg.cuh", "tma.cuh"] + _COMMON),
     "dft_rows": (r"\bdft_rows_gemm_kernel<[0-9]+, [0-9]+, true", ["stages_dft.cu"] + _COMMON),
     "dft_irows": (r"\bdft_rows_gemm_kernel<[0-9]+, [0-9]+, false", ["stages_dft.cu"] + _COMMON),
     "dft_cols": (r"\bdft_cols_gemm_kernel<true>", ["stages_dft.cu"] + _COMMON),
@@ -412,6 +417,8 @@ def run_ours(args, cfg):
 
     peaks, peak_kind = read_peaks()
     plan = fnospec.Plan(cfg.B, cfg.Cin, cfg.Cout, cfg.H, cfg.W, cfg.m1, cfg.m2, args.precision)
+    if args.single_launch != "auto":
+        plan.fno_plan_set_single_launch(args.single_launch == "on")
     step_bytes = cfg.algorithmic_bytes()
     # rotate over enough distinct (x, w, y) sets that no buffer is still in L2
     # when it is used again (every step touches a different set)
@@ -931,6 +938,9 @@ def main():
                          "(any H, W in [2, 4096]); x ~ N(0,1), w ~ U[0,1)/(Cin*Cout)")
     ap.add_argument("--shape1d", default="64,64,64,4096,64",
                     help="B,Cin,Cout,L,m of the 1D layer (--pass layer1d)")
+    ap.add_argument("--single-launch", default="auto", choices=["auto", "on", "off"],
+                    help="run the layer as one cooperative launch (on), as three launches "
+                         "(off), or as the plan chooses (auto)")
     ap.add_argument("--ingest-ncu", metavar="CSV", default=None,
                     help="record the DRAM bytes per launch of an ncu --csv capture of this "
                          "workload (metrics dram__bytes_read.sum, dram__bytes_write.sum) in "

@@ -158,6 +158,18 @@ void describe_1d(fno_plan_s* p) {
     p->launches = 3;
 }
 
+// Kernel list of the single-launch layer (layer_persistent.cu), or of the
+// regular path when single_launch is off.
+void describe_launches(fno_plan_s* p) {
+    if (p->single_launch) {
+        set_kernel(p, 0, "layer_persistent", x_bytes(p) + w_bytes(p) + y_bytes(p),
+                   8ull * p->B * p->Cin * p->Cout * p->nm);
+        p->launches = 1;
+    } else {
+        describe_fused(p);
+    }
+}
+
 cudaError_t run_forward(const fno_plan_s& p, const float* x, float2* X, float2* T, cudaStream_t s,
                         fno_launch_ctx* ctx) {
     if (p.dims == 1)
@@ -215,6 +227,7 @@ cudaError_t init_device() {
     if (e == cudaSuccess) e = block_init();
     if (e == cudaSuccess) e = mix_tc_init();
     if (e == cudaSuccess) e = mix_tcm_init();
+    if (e == cudaSuccess) e = layer_persistent_init();
     if (e == cudaSuccess) g_init_done[dev] = true;
     return e;
 }
@@ -347,6 +360,10 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
         std::snprintf(p->desc, sizeof(p->desc),
                       "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|%s|inv-cols+rows(R=%d,P=%d)", W,
                       p->R, p->P, mix_name(p), p->Ri, p->Pi);
+        // the single-launch layer (fno_plan_set_single_launch) is opt-in: measured
+        // slower than the three launches with programmatic dependent launch at
+        // every shape it serves (64x64 B8 C32: 38.7 against 18.6 us; 128x128
+        // B16 C64: 187 against 83 us)
     } else if (dft_path(H, W)) {
         describe_generic(p);
         std::snprintf(p->kernels[0].name, sizeof(p->kernels[0].name), "dft_rows");
@@ -374,6 +391,8 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
     if (e == cudaSuccess) e = cudaMalloc(&p->tw_w, sizeof(float2) * W);
     // err[0]: error bits, err[1]: debug flags (see fno_plan_debug_force_timeout)
     if (e == cudaSuccess) e = cudaMalloc(&p->err, 2 * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMalloc(&p->gbar, sizeof(unsigned long long));
+    if (e == cudaSuccess) e = cudaMemset(p->gbar, 0, sizeof(unsigned long long));
     if (e == cudaSuccess) e = cudaMemcpy(p->tw_h, th.data(), sizeof(float2) * H, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(p->tw_w, tw.data(), sizeof(float2) * W, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(p->err, 0, 2 * sizeof(unsigned));
@@ -435,6 +454,7 @@ fno_status_t fno_plan_destroy(fno_plan_t p) {
         if (p->tw_h) cudaFree(p->tw_h);
         if (p->tw_w) cudaFree(p->tw_w);
         if (p->err) cudaFree(p->err);
+        if (p->gbar) cudaFree(p->gbar);
     }
     delete p;
     return FNO_OK;
@@ -512,6 +532,11 @@ fno_status_t fno_plan_execute(fno_plan_t p, const float* x, const void* w, float
     ctx.events = p->events;
     ctx.count = p->nevents;
     cudaError_t e = ctx.mark(s);
+    if (p->single_launch) {
+        if (e == cudaSuccess)
+            e = launch_layer_persistent(*p, x, static_cast<const float2*>(w), y, X, Z, s, &ctx);
+        return cuda_status(e);
+    }
     if (e == cudaSuccess) e = run_forward(*p, x, X, T, s, &ctx);
     if (e == cudaSuccess) e = run_mix(*p, X, static_cast<const float2*>(w), Z, s, &ctx, true);
     if (e == cudaSuccess) e = run_inverse(*p, Z, y, T, s, &ctx);
@@ -617,6 +642,22 @@ fno_status_t fno_plan_debug_force_timeout(fno_plan_t p, int enable) {
     const unsigned flags = enable ? 1u : 0u;
     if (cudaMemcpy(p->err + 1, &flags, sizeof(flags), cudaMemcpyHostToDevice) != cudaSuccess)
         return FNO_ERR_CUDA;
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_set_single_launch(fno_plan_t p, int enable) {
+    if (!p || p->adjoint) return FNO_ERR_INVALID_ARG;
+    if (enable && !layer_persistent_supported(*p)) return FNO_ERR_UNSUPPORTED;
+    if (p->events) return FNO_ERR_INVALID_ARG;  // armed events are sized for the launch count
+    p->single_launch = enable ? 1 : 0;
+    describe_launches(p);
+    if (p->single_launch)
+        std::snprintf(p->desc, sizeof(p->desc), "single-launch: fwd-fused(W=%d)|mix|inv-fused",
+                      p->W);
+    else
+        std::snprintf(p->desc, sizeof(p->desc),
+                      "fused: fwd-rows+cols(W=%d,R=%d,P=%d)|%s|inv-cols+rows(R=%d,P=%d)", p->W,
+                      p->R, p->P, mix_name(p), p->Ri, p->Pi);
     return FNO_OK;
 }
 

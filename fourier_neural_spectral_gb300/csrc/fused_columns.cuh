@@ -116,12 +116,16 @@ __device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, in
 // sum of Z over the retained k1 == f (mod R), each times e^{+2 pi i k1 p / H}
 // (P = 1: the single retained frequency k1 = f, if any).  `cup` is
 // e^{+2 pi i (H - R) p / H}, the ratio of the upper-side twiddle to the lower.
-// ZS: Z is in shared memory (plain loads) rather than global memory.
-template <int R, bool ZS>
+// ZS: Z is in shared memory (plain loads) rather than global memory.  COH: Z
+// in global memory was written earlier in the same launch by other CTAs, so it
+// is read through L2 (ld.global.cg) instead of the read-only path.
+template <int R, bool ZS, bool COH = false>
 __device__ __forceinline__ float2 gather_residue(const float2* Zp, int f, int col, int H, int m1,
                                                  int m2, int P, int p, float2 cup,
                                                  const float2* __restrict__ tw_h) {
-    const auto ld = [&](size_t i) { return ZS ? Zp[i] : __ldg(&Zp[i]); };
+    const auto ld = [&](size_t i) {
+        return ZS ? Zp[i] : (COH ? __ldcg(&Zp[i]) : __ldg(&Zp[i]));
+    };
     float2 val = make_float2(0.f, 0.f);
     if (P == 1) {
         int kf;
@@ -145,7 +149,7 @@ __device__ __forceinline__ float2 gather_residue(const float2* Zp, int f, int co
 // ZS = true: Zp points to the plane's Z in shared memory, overlapping scr and V;
 // requires a single pass (m2 <= ColCfg<R>::CP).  Every thread reads its inputs
 // before the first barrier, after which the scratch and V may be rewritten.
-template <int R, int M1S = 0, bool ZS = false>
+template <int R, int M1S = 0, bool ZS = false, bool COH = false>
 __device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys, const float2* Zp,
                                                 int H, int m1, int m2, int P, int p,
                                                 const float2* __restrict__ tw_h) {
@@ -166,7 +170,7 @@ __device__ __forceinline__ void columns_inverse(float2* scr, float2* V, int ys, 
 #pragma unroll
             for (int k1 = 0; k1 < Bq; ++k1)
                 u[k1] = k1_live<R, M1S>(k1)
-                            ? gather_residue<R, ZS>(Zp, 16 * k1 + t + Bq * j, col, H, m1, m2, P, p,
+                            ? gather_residue<R, ZS, COH>(Zp, 16 * k1 + t + Bq * j, col, H, m1, m2, P, p,
                                                     cup, tw_h)
                             : make_float2(0.f, 0.f);
         };

@@ -63,6 +63,8 @@ struct fno_plan_s {
     float2* tw_h;           // e^{+2 pi i j / H}, j in [0, H)
     float2* tw_w;           // e^{+2 pi i j / W}, j in [0, W)
     unsigned* err;          // device error word
+    unsigned long long* gbar;  // grid-barrier counter of the single-launch layer
+    int single_launch;      // execute runs the whole layer as one launch
     // workspace layout (byte offsets, each 256-byte aligned)
     size_t off_X, off_Z, off_T, ws_bytes;
     int path;               // 0: shape-generic kernels, 1: fused transform kernels
@@ -151,6 +153,13 @@ bool mix_tcm_supported(int B, int Cin, int Cout, int nm);
 cudaError_t launch_mix_tcm(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
                            int split, bool after_own_forward, cudaStream_t s,
                            fno_launch_ctx* ctx);
+
+// The whole layer in one cooperative launch (layer_persistent.cu).
+cudaError_t layer_persistent_init();
+bool layer_persistent_supported(const fno_plan_s& p);
+cudaError_t launch_layer_persistent(const fno_plan_s& p, const float* x, const float2* w,
+                                    float* y, float2* X, float2* Z, cudaStream_t s,
+                                    fno_launch_ctx* ctx);
 
 // Direct-DFT transforms for H or W not a power of two (stages_dft.cu); the
 // shape-generic launchers below route such shapes there.

@@ -39,7 +39,7 @@ EXPORTS = (
     "fno_release_cache", "fno_forward_modes", "fno_mix_modes", "fno_inverse_modes",
     "fno_get_device_status", "fno_spectral_conv2d_noalloc", "fno_plan_backward",
     "fno_block_epilogue", "fno_block_execute", "fno_plan_create_1d",
-    "fno_plan_debug_force_timeout",
+    "fno_plan_debug_force_timeout", "fno_plan_set_single_launch",
 )
 
 
@@ -71,6 +71,7 @@ def load_library(path: str = LIB_PATH):
             "fno_plan_create": (st, [ctypes.POINTER(vp), i, i, i, i, i, i, i, i]),
             "fno_plan_create_1d": (st, [ctypes.POINTER(vp), i, i, i, i, i, i]),
             "fno_plan_debug_force_timeout": (st, [vp, i]),
+            "fno_plan_set_single_launch": (st, [vp, i]),
             "fno_plan_workspace_size": (st, [vp, ctypes.POINTER(sz)]),
             "fno_plan_launch_count": (st, [vp, ctypes.POINTER(i)]),
             "fno_plan_describe": (st, [vp, ctypes.c_char_p, sz]),
@@ -160,6 +161,16 @@ class Plan:
         n = ctypes.c_size_t()
         _check(lib.fno_plan_workspace_size(h, ctypes.byref(n)), "fno_plan_workspace_size")
         self.workspace_bytes = int(n.value)
+        self._describe()
+        self._event_array = None
+        self.workspace = None
+        if allocate_workspace and self.workspace_bytes:
+            self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device="cuda")
+
+    def _describe(self):
+        """Launch count, description and kernel list of the plan as it stands."""
+        lib = load_library()
+        h = self._h
         k = ctypes.c_int()
         _check(lib.fno_plan_launch_count(h, ctypes.byref(k)), "fno_plan_launch_count")
         self.launches = int(k.value)
@@ -174,10 +185,6 @@ class Plan:
                    "fno_plan_kernel_info")
             self.kernels.append({"name": nm.value.decode(), "bytes": int(nb.value),
                                  "flops": int(nf.value)})
-        self._event_array = None
-        self.workspace = None
-        if allocate_workspace and self.workspace_bytes:
-            self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device="cuda")
 
     @property
     def handle(self):
@@ -256,6 +263,14 @@ class Plan:
         (see include/fnospec.h)."""
         _check(load_library().fno_plan_debug_force_timeout(self._h, 1 if enable else 0),
                "fno_plan_debug_force_timeout")
+
+    def fno_plan_set_single_launch(self, enable: bool):
+        """Run execute as one cooperative launch (True) or three (False); the
+        launch count, kernel list and description follow."""
+        lib = load_library()
+        _check(lib.fno_plan_set_single_launch(self._h, 1 if enable else 0),
+               "fno_plan_set_single_launch")
+        self._describe()
 
     def fno_get_device_status(self, stream=None) -> int:
         return int(load_library().fno_get_device_status(self._h, _stream(stream)))

@@ -258,6 +258,24 @@ fno_status_t fno_spectral_conv2d_noalloc(const float* x, const void* w, float* y
                                          int Cin, int Cout, int H, int W, int m1, int m2,
                                          cudaStream_t s);
 
+/* Choose how fno_plan_execute runs the layer: enable != 0 runs the whole layer
+ * as ONE cooperative launch (forward transforms, per-mode contraction and
+ * inverse transforms as three phases of one persistent grid, separated by
+ * grid-wide barriers; the retained spectra cross CTAs through the plan's
+ * workspace inside the launch), enable = 0 as the regular three launches.  This
+ * is the fused FFT -> GEMM -> iFFT operator of the TurboFNO page, sections 1
+ * and 2.1-2.3 (no launch between the stages).  Served for square planes
+ * H = W in {32, 64, 128, 256} with batch up to 16 (FNO_ERR_UNSUPPORTED
+ * otherwise).  Plans start with it off: the three launches, which overlap
+ * one another's start and end through programmatic dependent launch, are the
+ * faster form at every shape it serves.  Host-only; changes
+ * fno_plan_launch_count, so call it before fno_plan_record_events
+ * (FNO_ERR_INVALID_ARG while events are armed, for a NULL plan or for a
+ * backward's internal plan).  The grid barriers wait at most one second; a
+ * wait that runs out is reported by fno_get_device_status as FNO_ERR_TIMEOUT.
+ * Calls that use the same plan must not overlap on the GPU. */
+fno_status_t fno_plan_set_single_launch(fno_plan_t plan, int enable);
+
 /* Synchronise stream s, read and clear the plan's device error word.  Returns
  * FNO_OK, FNO_ERR_TIMEOUT or FNO_ERR_DEVICE (or FNO_ERR_CUDA if the copy fails).
  * This is the stage-by-stage fault check of the FFT operator-optimisation page,
