@@ -138,8 +138,8 @@ KERNEL_SOURCES = {
     "mix_tma": (r"\bmix_tma_kernel\b", ["mix_tma.cu", "tma.cuh"] + _COMMON),
     "mix_tc_tf32": (r"\bmix_tc_kernel<1>", ["mix_tc.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
     "mix_tc_3xtf32": (r"\bmix_tc_kernel<3>", ["mix_tc.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
-    "mix_tcm_3xtf32": (r"\bmix_tcm_kernel<3", ["mix_tcm.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
-    "mix_tcm_tf32": (r"\bmix_tcm_kernel<1", ["mix_tcm.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
+    "mix_tcm_3xtf32": (r"\bmix_tcm_kernel<\d+, 3>", ["mix_tcm.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
+    "mix_tcm_tf32": (r"\bmix_tcm_kernel<\d+, 1>", ["mix_tcm.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
     "layer_persistent": (r"\blayer_persistent_kernel\b",
                          ["layer_persistent.cu", "fused_rows.cuh", "fused_columns.cuh",
                           "fft_reg.cuh", "tma.cuh"] + _COMMON),

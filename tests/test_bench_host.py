@@ -81,6 +81,23 @@ def test_traffic_ingest_and_stale_sources(tmp_path):
     assert bench.measured_traffic("W", k0, "fp32", path=str(out)) is None
 
 
+def test_kernel_patterns_pick_one_name_each():
+    import re
+    import bench
+    demangled = {
+        "mix_tcm_kernel<16, 3>": "mix_tcm_3xtf32", "mix_tcm_kernel<8, 1>": "mix_tcm_tf32",
+        "mix_tc_kernel<3>": "mix_tc_3xtf32", "mix_tc_kernel<1>": "mix_tc_tf32",
+        "fwd_fused_kernel<128, 128, 32, 32>": "fwd_fused", "inv_big_kernel<2048, 64, true>":
+        "inv_fused", "mix_wide_kernel<16, 0>": "mix_wide", "layer_persistent_kernel<64, 16, 16>":
+        "layer_persistent", "dft_rows_gemm_kernel<64, 4, true, true>": "dft_rows",
+        "dft_rows_gemm_kernel<64, 2, false, false>": "dft_irows",
+    }
+    for name, want in demangled.items():
+        hits = [k for k, (rx, _) in bench.KERNEL_SOURCES.items()
+                if re.search(rx, "void fno::(anonymous namespace)::" + name + "(...)")]
+        assert hits == [want], (name, hits)
+
+
 def test_committed_traffic_file_parses():
     import json
     import bench
