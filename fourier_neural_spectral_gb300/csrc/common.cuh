@@ -24,6 +24,47 @@ __device__ __forceinline__ void cmac(float2& acc, float2 a, float2 b) {
 
 __device__ __forceinline__ int ilog2(int v) { return 31 - __clz(v); }
 
+// Range-checked builds (compiled with -DFNO_DEBUG, the library
+// libfnospec_debug.so): every global store of the kernels that take
+// FNO_DBG_PARAM is checked against the output ranges of its launch; a store
+// outside them is skipped and sets bit 0 (FNO_DEVERR_BOUNDS) of the plan's
+// device error word, which fno_get_device_status reports as FNO_ERR_DEVICE.
+// Nothing traps or faults.  A kernel passes FNO_DBG_PARAM last in its
+// parameter list, calls FNO_DBG_BEGIN() before any role split (it publishes
+// the ranges to the CTA through shared memory with one barrier), and guards
+// each store with FNO_DBG_OK(address, bytes).  Without FNO_DEBUG the three
+// macros vanish and the kernels compile exactly as without them.
+#ifdef FNO_DEBUG
+struct fno_dbg_ranges {
+    const char* lo[2];
+    const char* hi[2];
+    unsigned* err;
+};
+__device__ __forceinline__ fno_dbg_ranges& fno_dbg() {
+    __shared__ fno_dbg_ranges r;
+    return r;
+}
+__device__ __forceinline__ bool fno_dbg_check(const void* p, size_t bytes) {
+    const char* a = static_cast<const char*>(p);
+    const fno_dbg_ranges& r = fno_dbg();
+    for (int k = 0; k < 2; ++k)
+        if (r.lo[k] && a >= r.lo[k] && a + bytes <= r.hi[k]) return true;
+    if (r.err) atomicOr(r.err, 1u /* FNO_DEVERR_BOUNDS */);
+    return false;
+}
+#define FNO_DBG_PARAM , fno::fno_dbg_ranges fno_dbg_in
+#define FNO_DBG_BEGIN()                                   \
+    do {                                                  \
+        if (threadIdx.x == 0) fno::fno_dbg() = fno_dbg_in; \
+        __syncthreads();                                  \
+    } while (0)
+#define FNO_DBG_OK(p, bytes) fno::fno_dbg_check((p), (bytes))
+#else
+#define FNO_DBG_PARAM
+#define FNO_DBG_BEGIN() ((void)0)
+#define FNO_DBG_OK(p, bytes) true
+#endif
+
 // Programmatic dependent launch (PTX griddepcontrol, sm_90+).  Kernels of the
 // layer's main path are launched with programmatic stream serialisation
 // (launch_pdl in internal.h) and begin with

@@ -645,6 +645,18 @@ fno_status_t fno_plan_debug_force_timeout(fno_plan_t p, int enable) {
     return FNO_OK;
 }
 
+fno_status_t fno_plan_debug_bounds_margin(fno_plan_t p, size_t bytes) {
+    if (!p || p->adjoint) return FNO_ERR_INVALID_ARG;
+#ifdef FNO_DEBUG
+    p->dbg_margin = bytes;
+    if (p->adj) p->adj->dbg_margin = bytes;
+    return FNO_OK;
+#else
+    (void)bytes;
+    return FNO_ERR_UNSUPPORTED;  // only the range-checked build checks stores
+#endif
+}
+
 fno_status_t fno_plan_set_single_launch(fno_plan_t p, int enable) {
     if (!p || p->adjoint) return FNO_ERR_INVALID_ARG;
     if (enable && !layer_persistent_supported(*p)) return FNO_ERR_UNSUPPORTED;

@@ -81,29 +81,31 @@ __device__ __forceinline__ void columns_forward(float2* scr, const float2* Y, in
                     if (P == 1) {
                         int kf;
                         const int r = row_of_residue(f, R, H, m1, &kf);
-                        if (r >= 0) X[xbase + (size_t)r * m2 + col] = val;
+                        if (r >= 0 && FNO_DBG_OK(&X[xbase + (size_t)r * m2 + col], sizeof(float2)))
+                            X[xbase + (size_t)r * m2 + col] = val;
                     } else if (m1 <= R) {
                         // at most one retained frequency per side: lower k1 = f, upper
                         // k1 = H - R + f, whose twiddle is the lower one times cdn
                         const bool lo = f < m1, hi = f >= R - m1;
                         if (!lo && !hi) continue;
                         const float2 a = cmul(val, root<-1>(tw_h, f * p, H));
-                        if (lo)
-                            atomicAdd(reinterpret_cast<float2*>(X + xbase + (size_t)f * m2 + col), a);
-                        if (hi)
-                            atomicAdd(reinterpret_cast<float2*>(
-                                          X + xbase + (size_t)(f - R + 2 * m1) * m2 + col),
-                                      cmul(a, cdn));
+                        float2* xl = X + xbase + (size_t)f * m2 + col;
+                        float2* xh = X + xbase + (size_t)(f - R + 2 * m1) * m2 + col;
+                        if (lo && FNO_DBG_OK(xl, sizeof(float2))) atomicAdd(xl, a);
+                        if (hi && FNO_DBG_OK(xh, sizeof(float2))) atomicAdd(xh, cmul(a, cdn));
                     } else {
                         // every retained k1 == f (mod R): lower side f, f + R, ... < m1,
                         // upper side H - R + f, H - 2R + f, ... >= H - m1
-                        for (int kf = f; kf < m1; kf += R)
-                            atomicAdd(reinterpret_cast<float2*>(X + xbase + (size_t)kf * m2 + col),
-                                      cmul(val, root<-1>(tw_h, kf * p, H)));
-                        for (int kf = H - R + f; kf >= H - m1; kf -= R)
-                            atomicAdd(reinterpret_cast<float2*>(
-                                          X + xbase + (size_t)(kf - H + 2 * m1) * m2 + col),
-                                      cmul(val, root<-1>(tw_h, kf * p, H)));
+                        for (int kf = f; kf < m1; kf += R) {
+                            float2* xa = X + xbase + (size_t)kf * m2 + col;
+                            if (FNO_DBG_OK(xa, sizeof(float2)))
+                                atomicAdd(xa, cmul(val, root<-1>(tw_h, kf * p, H)));
+                        }
+                        for (int kf = H - R + f; kf >= H - m1; kf -= R) {
+                            float2* xa = X + xbase + (size_t)(kf - H + 2 * m1) * m2 + col;
+                            if (FNO_DBG_OK(xa, sizeof(float2)))
+                                atomicAdd(xa, cmul(val, root<-1>(tw_h, kf * p, H)));
+                        }
                     }
                 }
             }

@@ -284,8 +284,8 @@ __device__ __forceinline__ void row_pair_inverse(const float2* Va, const float2*
         dft<16, 1>(v);
 #pragma unroll
         for (int n2 = 0; n2 < 16; ++n2) {
-            ya[t + Bq * n2] = v[n2].x;
-            yb[t + Bq * n2] = v[n2].y;
+            if (FNO_DBG_OK(&ya[t + Bq * n2], sizeof(float))) ya[t + Bq * n2] = v[n2].x;
+            if (FNO_DBG_OK(&yb[t + Bq * n2], sizeof(float))) yb[t + Bq * n2] = v[n2].y;
         }
     }
     __syncwarp();

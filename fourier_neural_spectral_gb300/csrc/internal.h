@@ -6,6 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "common.cuh"
 #include "fnospec.h"
 
 // Bits of the device error word.
@@ -30,6 +31,35 @@ struct fno_launch_ctx {
         return cudaEventRecord(events[next++], s);
     }
 };
+
+// Dynamic shared memory one block may ask for: the opt-in limit (227 KB), less
+// room for the static shared memory (the output ranges) that range-checked
+// builds add to their kernels.
+#ifdef FNO_DEBUG
+constexpr size_t kMaxDynSmem = 227 * 1024 - 1024;
+#else
+constexpr size_t kMaxDynSmem = 227 * 1024;
+#endif
+
+// The output ranges a range-checked build checks a launch's stores against:
+// FNO_DBG_ARG1(ptr, bytes, plan) for one output, FNO_DBG_ARG2 for two.  The
+// first range is shortened by the plan's debug margin (the test hook that
+// makes the last outputs count as out of range).  Empty without FNO_DEBUG.
+#ifdef FNO_DEBUG
+#define FNO_DBG_RANGES2(p0, n0, p1, n1, plan)                                                \
+    fno::fno_dbg_ranges {                                                                     \
+        {((const char*)(const void*)(p0)), ((const char*)(const void*)(p1))},             \
+            {((const char*)(const void*)(p0)) +                                              \
+                 ((size_t)(n0) > (plan).dbg_margin ? (size_t)(n0) - (plan).dbg_margin : 0),  \
+             ((const char*)(const void*)(p1)) + (n1)},                                      \
+            (plan).err                                                                        \
+    }
+#define FNO_DBG_ARG2(p0, n0, p1, n1, plan) , FNO_DBG_RANGES2(p0, n0, p1, n1, plan)
+#define FNO_DBG_ARG1(p0, n0, plan) FNO_DBG_ARG2(p0, n0, nullptr, 0, plan)
+#else
+#define FNO_DBG_ARG2(p0, n0, p1, n1, plan)
+#define FNO_DBG_ARG1(p0, n0, plan)
+#endif
 
 // Launch with programmatic stream serialisation (the kernel must call
 // griddep_wait() before touching memory that earlier kernels of the stream
@@ -65,6 +95,8 @@ struct fno_plan_s {
     unsigned* err;          // device error word
     unsigned long long* gbar;  // grid-barrier counter of the single-launch layer
     int single_launch;      // execute runs the whole layer as one launch
+    size_t dbg_margin;      // range-checked builds: bytes taken off each launch's first
+                            // output range (fno_plan_debug_bounds_margin)
     // workspace layout (byte offsets, each 256-byte aligned)
     size_t off_X, off_Z, off_T, ws_bytes;
     int path;               // 0: shape-generic kernels, 1: fused transform kernels

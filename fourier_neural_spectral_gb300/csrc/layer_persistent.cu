@@ -129,7 +129,8 @@ __device__ __forceinline__ void mix_unit(unsigned char* smem, const float2* X,
     if (m < NM && o < Cout) {
 #pragma unroll
         for (int b = 0; b < kUB; ++b)
-            if (b < B) Z[((size_t)b * Cout + o) * NM + m] = acc[b];
+            if (b < B && FNO_DBG_OK(&Z[((size_t)b * Cout + o) * NM + m], sizeof(float2)))
+                Z[((size_t)b * Cout + o) * NM + m] = acc[b];
     }
 }
 
@@ -139,7 +140,8 @@ layer_persistent_kernel(const float* __restrict__ x, const float2* __restrict__ 
                         float* __restrict__ y, float2* X, float2* Z, int B, int Cin, int Cout,
                         int m1, int m2, float scale, const float2* __restrict__ tw_w,
                         const float2* __restrict__ tw_h, unsigned long long* gbar,
-                        unsigned* __restrict__ err) {
+                        unsigned* __restrict__ err FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     constexpr int H = W, R = W;  // square planes, one column pass
     using C = FusedCfg<W, R>;
     extern __shared__ __align__(16) float2 sm[];
@@ -211,8 +213,18 @@ cudaError_t launch_one(const fno_plan_s& p, const float* x, const float2* w, flo
     const float2* tw_h = p.tw_h;
     unsigned long long* gbar = p.gbar;
     unsigned* err = p.err;
+#ifdef FNO_DEBUG
+    // the spectra X and Z are adjacent in the workspace: one range covers both
+    fno_dbg_ranges dbg = FNO_DBG_RANGES2(
+        X, (size_t)((const char*)Z - (const char*)X) + 8ull * p.B * p.Cout * p.nm, y,
+        4ull * p.B * p.Cout * p.H * p.W, p);
+    void* args[] = {(void*)&x, (void*)&w, (void*)&y, (void*)&X, (void*)&Z, &B, &Cin, &Cout,
+                    &m1, &m2, &scale, (void*)&tw_w, (void*)&tw_h, (void*)&gbar, (void*)&err,
+                    (void*)&dbg};
+#else
     void* args[] = {(void*)&x, (void*)&w, (void*)&y, (void*)&X, (void*)&Z, &B, &Cin, &Cout,
                     &m1, &m2, &scale, (void*)&tw_w, (void*)&tw_h, (void*)&gbar, (void*)&err};
+#endif
     return cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kPT), args, smem, s);
 }
 

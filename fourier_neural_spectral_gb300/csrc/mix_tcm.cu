@@ -116,7 +116,8 @@ template <int BP, int SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 mix_tcm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                float2* __restrict__ Z, int B, int Cin, int Cout, int NM, int early_w,
-               unsigned* __restrict__ err) {
+               unsigned* __restrict__ err FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     using C = TcmCfg<BP>;
     constexpr int N = C::N;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -430,7 +431,8 @@ mix_tcm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     const int b = r / kOB, og = o0 + (r - b * kOB), mg = m0 + 2 * j;
                     const float4 v =
                         *reinterpret_cast<const float4*>(zst + swz64((uint32_t)r, (uint32_t)j));
-                    if (b < B && og < Cout && mg < NM)
+                    if (b < B && og < Cout && mg < NM &&
+                        FNO_DBG_OK(Z + ((size_t)b * Cout + og) * NM + mg, 2 * sizeof(float2)))
                         *reinterpret_cast<float4*>(Z + ((size_t)b * Cout + og) * NM + mg) = v;
                 }
             }
@@ -477,7 +479,8 @@ cudaError_t launch_bp(const fno_plan_s& p, const float2* X, const float2* w, flo
     const int units = ((p.nm + kQM - 1) / kQM) * ((p.Cout + kOB - 1) / kOB);
     const int grid = units < p.sms ? units : p.sms;
     return launch_pdl(mix_tcm_kernel<BP, SPLIT>, dim3(grid), dim3(kThreads), TcmCfg<BP>::Smem, s,
-                      mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, early_w, p.err);
+                      mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, early_w, p.err
+                      FNO_DBG_ARG1(Z, 8ull * p.B * p.Cout * p.nm, p));
 }
 
 }  // namespace

@@ -99,7 +99,8 @@ template <int BT, int MODE>
 __global__ void __launch_bounds__(WideTile<BT>::Threads, WideTile<BT>::MinBlocks)
 mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 float2* __restrict__ Z, int rows, int red, int Cout, int NM, int m2, int W,
-                int early_w, unsigned* __restrict__ err) {
+                int early_w, unsigned* __restrict__ err FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     using T = WideTile<BT>;
     constexpr int JB = T::JB, IC = T::IC, kOCB = T::OCB, kJO = T::JO, kNST = T::NST;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -234,7 +235,9 @@ mix_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
         for (int bb = 0; bb < JB; ++bb) {
             const int r = b0 + bh * JB + bb;
             if (r >= rows) break;
-            Z[((size_t)r * Cout + o) * NM + m] = MODE == kWgrad ? cscale(acc[j][bb], c) : acc[j][bb];
+            if (FNO_DBG_OK(&Z[((size_t)r * Cout + o) * NM + m], sizeof(float2)))
+                Z[((size_t)r * Cout + o) * NM + m] =
+                    MODE == kWgrad ? cscale(acc[j][bb], c) : acc[j][bb];
         }
     }
 }
@@ -266,9 +269,10 @@ cudaError_t launch_bt(const CUtensorMap& mw, const CUtensorMap& mx, float2* Z, c
     if (p.adjoint)
         return launch_pdl(mix_wide_kernel<BT, kAdj>, grid, WideTile<BT>::Threads,
                           WideTile<BT>::Smem, s, mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W,
-                          early_w, p.err);
+                          early_w, p.err FNO_DBG_ARG1(Z, 8ull * p.B * p.Cout * p.nm, p));
     return launch_pdl(mix_wide_kernel<BT, kMix>, grid, WideTile<BT>::Threads, WideTile<BT>::Smem,
-                      s, mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, early_w, p.err);
+                      s, mw, mx, Z, p.B, p.Cin, p.Cout, p.nm, p.m2, p.W, early_w, p.err
+                      FNO_DBG_ARG1(Z, 8ull * p.B * p.Cout * p.nm, p));
 }
 
 // 3D tensor map over a complex64 array [d2][d1][NM] viewed as floats: dims
@@ -305,7 +309,7 @@ cudaError_t mix_wide_init() {
 bool mix_wide_supported(int B, int Cin, int Cout, int nm) {
     (void)Cout;
     if (nm < kModes || (nm & 1) || B < 1 || Cin < 1) return false;
-    return wide_smem(wide_bt(B)) <= 227 * 1024;
+    return wide_smem(wide_bt(B)) <= kMaxDynSmem;
 }
 
 cudaError_t launch_mix_wide(const fno_plan_s& p, const float2* X, const float2* w, float2* Z,
@@ -364,5 +368,6 @@ cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2
                     (p.Cin + 15) / 16);
     // G comes from an earlier kernel than the forward stage just before this one
     return launch_pdl(mix_wide_kernel<16, kWgrad>, grid, T::Threads, T::Smem, s, mg, mx, gw,
-                      p.Cin, p.B, p.Cout, p.nm, p.m2, p.W, 1, p.err);
+                      p.Cin, p.B, p.Cout, p.nm, p.m2, p.W, 1, p.err
+                      FNO_DBG_ARG1(gw, 8ull * p.Cin * p.Cout * p.nm, p));
 }

@@ -116,7 +116,8 @@ template <int W, int R>
 __global__ void __launch_bounds__(kBT, 2)
 fwd_big_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m1, int m2, int P,
                float scale, const float2* __restrict__ tw_w, const float2* __restrict__ tw_h,
-               unsigned* __restrict__ err) {
+               unsigned* __restrict__ err FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     using B = BigCfg<W>;
     constexpr int L = B::L, G = B::G, NK = B::NK;
     constexpr uint32_t kRowBytes = W * sizeof(float);
@@ -243,7 +244,8 @@ template <int W, int R, bool ZS>
 __global__ void __launch_bounds__(kBT, 2)
 inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m1, int m2, int P,
                float scale, const float2* __restrict__ tw_w, const float2* __restrict__ tw_h,
-               unsigned* __restrict__ err) {
+               unsigned* __restrict__ err FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     using B = BigCfg<W>;
     constexpr int L = B::L, G = B::G, NK = B::NK;
     constexpr int half = W / 2;
@@ -336,8 +338,8 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
             float* yb = ya + (size_t)P * W;
 #pragma unroll
             for (int n2 = 0; n2 < 16; ++n2) {
-                ya[t + L * n2] = v[n2].x;
-                yb[t + L * n2] = v[n2].y;
+                if (FNO_DBG_OK(&ya[t + L * n2], sizeof(float))) ya[t + L * n2] = v[n2].x;
+                if (FNO_DBG_OK(&yb[t + L * n2], sizeof(float))) yb[t + L * n2] = v[n2].y;
             }
         }
         group_sync<L>(g);
@@ -355,7 +357,8 @@ inv_big_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m
 template <int W>
 __global__ void __launch_bounds__(kBT, 2)
 fwd_rows1d_kernel(const float* __restrict__ x, float2* __restrict__ X, int S, int m2,
-                  float scale, const float2* __restrict__ tw_w) {
+                  float scale, const float2* __restrict__ tw_w FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     using B = BigCfg<W>;
     constexpr int L = B::L, G = B::G, NK = B::NK;
     __shared__ __align__(16) float2 scr[B::Groups * B::GroupScr];
@@ -415,8 +418,9 @@ fwd_rows1d_kernel(const float* __restrict__ x, float2* __restrict__ X, int S, in
             } else {
                 zm = Zs[(16 - kk) * NK + (L - 1 - k1) - L + 2 * kNL];
             }
-            X[(size_t)qa * m2 + k] = make_float2(hs * (zk.x + zm.x), hs * (zk.y - zm.y));
-            if (has_b)
+            if (FNO_DBG_OK(&X[(size_t)qa * m2 + k], sizeof(float2)))
+                X[(size_t)qa * m2 + k] = make_float2(hs * (zk.x + zm.x), hs * (zk.y - zm.y));
+            if (has_b && FNO_DBG_OK(&X[(size_t)(qa + 1) * m2 + k], sizeof(float2)))
                 X[(size_t)(qa + 1) * m2 + k] = make_float2(hs * (zk.y + zm.y), -hs * (zk.x - zm.x));
         }
     }
@@ -425,7 +429,8 @@ fwd_rows1d_kernel(const float* __restrict__ x, float2* __restrict__ X, int S, in
 template <int W>
 __global__ void __launch_bounds__(kBT, 2)
 inv_rows1d_kernel(const float2* __restrict__ Z, float* __restrict__ y, int S, int m2,
-                  float scale, const float2* __restrict__ tw_w) {
+                  float scale, const float2* __restrict__ tw_w FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     using B = BigCfg<W>;
     constexpr int L = B::L, G = B::G, NK = B::NK;
     constexpr int half = W / 2;
@@ -478,8 +483,8 @@ inv_rows1d_kernel(const float2* __restrict__ Z, float* __restrict__ y, int S, in
         float* yb = ya + W;
 #pragma unroll
         for (int n2 = 0; n2 < 16; ++n2) {
-            ya[t + L * n2] = v[n2].x;
-            if (has_b) yb[t + L * n2] = v[n2].y;
+            if (FNO_DBG_OK(&ya[t + L * n2], sizeof(float))) ya[t + L * n2] = v[n2].x;
+            if (has_b && FNO_DBG_OK(&yb[t + L * n2], sizeof(float))) yb[t + L * n2] = v[n2].y;
         }
     }
 }
@@ -491,8 +496,10 @@ cudaError_t launch_rows1d_w(const fno_plan_s& p, const float* x, float2* X, cons
     const int pairs = (S + 1) / 2;
     const unsigned grid = (unsigned)((pairs + BigCfg<W>::Groups - 1) / BigCfg<W>::Groups);
     if (FWD)
-        return launch_pdl(fwd_rows1d_kernel<W>, grid, kBT, 0, s, x, X, S, p.m2, p.scale, p.tw_w);
-    return launch_pdl(inv_rows1d_kernel<W>, grid, kBT, 0, s, Z, y, S, p.m2, p.scale, p.tw_w);
+        return launch_pdl(fwd_rows1d_kernel<W>, grid, kBT, 0, s, x, X, S, p.m2, p.scale, p.tw_w
+                          FNO_DBG_ARG1(X, 8ull * S * p.m2, p));
+    return launch_pdl(inv_rows1d_kernel<W>, grid, kBT, 0, s, Z, y, S, p.m2, p.scale, p.tw_w
+                      FNO_DBG_ARG1(y, 4ull * S * p.W, p));
 }
 
 template <bool FWD>
@@ -509,8 +516,8 @@ cudaError_t launch_rows1d(const fno_plan_s& p, const float* x, float2* X, const 
 
 template <int W, int R>
 cudaError_t set_attrs() {
-    const int fb = (int)std::min<size_t>(big_smem_bytes<W, R, true>(64), 227 * 1024);
-    const int ib = (int)std::min<size_t>(big_smem_bytes<W, R, false>(64), 227 * 1024);
+    const int fb = (int)std::min<size_t>(big_smem_bytes<W, R, true>(64), kMaxDynSmem);
+    const int ib = (int)std::min<size_t>(big_smem_bytes<W, R, false>(64), kMaxDynSmem);
     cudaError_t e =
         cudaFuncSetAttribute(fwd_big_kernel<W, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, fb);
     if (e == cudaSuccess)
@@ -538,15 +545,18 @@ cudaError_t launch(const fno_plan_s& p, const float* x, float2* X, const float2*
         const size_t smem = big_smem_bytes<W, R, true>(p.m2);
         const unsigned grid = (unsigned)((size_t)p.B * p.Cin * p.P);
         return launch_pdl(fwd_big_kernel<W, R>, grid, kBT, smem, s, x, X, p.H, p.m1, p.m2, p.P,
-                          p.scale, p.tw_w, p.tw_h, p.err);
+                          p.scale, p.tw_w, p.tw_h, p.err
+                          FNO_DBG_ARG1(X, 8ull * p.B * p.Cin * p.nm, p));
     } else {
         const size_t smem = big_smem_bytes<W, R, false>(p.m2);
         const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.Pi);
         if (big_z_staged<W, R>(p.m1, p.m2))
             return launch_pdl(inv_big_kernel<W, R, true>, grid, kBT, smem, s, Z, y, p.H, p.m1,
-                              p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
+                              p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err
+                              FNO_DBG_ARG1(y, 4ull * p.B * p.Cout * p.H * p.W, p));
         return launch_pdl(inv_big_kernel<W, R, false>, grid, kBT, smem, s, Z, y, p.H, p.m1, p.m2,
-                          p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
+                          p.Pi, p.scale, p.tw_w, p.tw_h, p.err
+                          FNO_DBG_ARG1(y, 4ull * p.B * p.Cout * p.H * p.W, p));
     }
 }
 

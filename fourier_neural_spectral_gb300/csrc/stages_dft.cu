@@ -66,7 +66,8 @@ template <int BN, int TM, bool FWD, bool GROUPED>
 __global__ void __launch_bounds__(kGT, (RowGemm<BN, TM>::MinBlocks))
 dft_rows_gemm_kernel(const float* __restrict__ A, float* __restrict__ C, long long M, int K,
                      int N, int W, float scale, const float2* __restrict__ tw, int ksplit,
-                     int kper) {
+                     int kper FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     using G = RowGemm<BN, TM>;
     __shared__ __align__(16) float As[2][kGBK][G::AS];
     __shared__ __align__(16) float Bs[2][kGBK][BN];
@@ -191,7 +192,8 @@ dft_rows_gemm_kernel(const float* __restrict__ A, float* __restrict__ C, long lo
         for (int g = 0; g < 2; ++g) {
             const int nb = n0 + (GROUPED ? g * (BN / 2) + tx * 4 : 0);
             if (vec && nb + 3 < N) {
-                *reinterpret_cast<float4*>(&Cr[nb]) =
+                if (FNO_DBG_OK(&Cr[nb], 4 * sizeof(float)))
+                    *reinterpret_cast<float4*>(&Cr[nb]) =
                     make_float4(acc[i][4 * g] * scale, acc[i][4 * g + 1] * scale,
                                 acc[i][4 * g + 2] * scale, acc[i][4 * g + 3] * scale);
                 continue;
@@ -200,7 +202,7 @@ dft_rows_gemm_kernel(const float* __restrict__ A, float* __restrict__ C, long lo
             for (int q = 0; q < 4; ++q) {
                 const int j = 4 * g + q;
                 const int nj = GROUPED ? nb + q : n0 + tx + G::NX * j;
-                if (nj < N) {
+                if (nj < N && FNO_DBG_OK(&Cr[nj], sizeof(float))) {
                     if (ksplit == 1) Cr[nj] = acc[i][j] * scale;
                     else atomicAdd(&Cr[nj], acc[i][j] * scale);
                 }
@@ -229,7 +231,8 @@ template <bool FWD>
 __global__ void __launch_bounds__(kCT)
 dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst, int M, int K,
                      long long ncols, int m2, int KB, int MC, int H, int m1, float alpha,
-                     const float2* __restrict__ tw_h) {
+                     const float2* __restrict__ tw_h FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     __shared__ __align__(16) float2 As[2][kCBK][kCBM];
     __shared__ __align__(16) float2 Bs[2][kCBK][kCBN];
     const int mtiles = (M + kCBM - 1) / kCBM;
@@ -326,7 +329,8 @@ dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int m = m0 + ty * 4 + i;
-            if (m < M) Cdst[((size_t)q * MC + m) * m2 + k2] = cscale(acc[i][j], alpha);
+            if (m < M && FNO_DBG_OK(&Cdst[((size_t)q * MC + m) * m2 + k2], sizeof(float2)))
+                Cdst[((size_t)q * MC + m) * m2 + k2] = cscale(acc[i][j], alpha);
         }
     }
 }
@@ -341,7 +345,7 @@ dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst,
 // varies from run to run.
 template <bool FWD>
 cudaError_t launch_rows_gemm(const float* A, float* C, long long M, int K, int N, int W,
-                             float scale, const float2* tw, cudaStream_t s) {
+                             float scale, const float2* tw, const fno_plan_s& p, cudaStream_t s) {
     constexpr long long kWant = 2 * 152;
     const auto tiles = [&](int bn, int bm) {
         return ((M + bm - 1) / bm) * (long long)((N + bn - 1) / bn);
@@ -378,27 +382,28 @@ cudaError_t launch_rows_gemm(const float* A, float* C, long long M, int K, int N
     const unsigned grid = (unsigned)(t * ksplit);
     if (cfg == 0)
         dft_rows_gemm_kernel<32, 4, FWD, true><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
-                                                                    ksplit, kper);
+                                                                    ksplit, kper FNO_DBG_ARG1(C, 4ull * M * N, p));
     else if (cfg == 1)
         dft_rows_gemm_kernel<64, 4, FWD, true><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
-                                                                    ksplit, kper);
+                                                                    ksplit, kper FNO_DBG_ARG1(C, 4ull * M * N, p));
     else if (cfg == 2)
         dft_rows_gemm_kernel<64, 2, FWD, true><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
-                                                                    ksplit, kper);
+                                                                    ksplit, kper FNO_DBG_ARG1(C, 4ull * M * N, p));
     else
         dft_rows_gemm_kernel<64, 2, FWD, false><<<grid, kGT, 0, s>>>(A, C, M, K, N, W, scale, tw,
-                                                                     ksplit, kper);
+                                                                     ksplit, kper FNO_DBG_ARG1(C, 4ull * M * N, p));
     return cudaGetLastError();
 }
 
 template <bool FWD>
 cudaError_t launch_cols_gemm(const float2* B, float2* C, int M, int K, long long planes, int m2,
                              int KB, int MC, int H, int m1, float alpha, const float2* tw_h,
-                             cudaStream_t s) {
+                             const fno_plan_s& p, cudaStream_t s) {
     const long long ncols = planes * m2;
     const long long grid = (long long)((M + kCBM - 1) / kCBM) * ((ncols + kCBN - 1) / kCBN);
-    dft_cols_gemm_kernel<FWD><<<(unsigned)grid, kCT, 0, s>>>(B, C, M, K, ncols, m2, KB, MC, H,
-                                                             m1, alpha, tw_h);
+    dft_cols_gemm_kernel<FWD><<<(unsigned)grid, kCT, 0, s>>>(
+        B, C, M, K, ncols, m2, KB, MC, H, m1, alpha, tw_h
+        FNO_DBG_ARG1(C, 8ull * planes * MC * m2, p));
     return cudaGetLastError();
 }
 
@@ -418,11 +423,11 @@ cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, f
                                cudaStream_t s, fno_launch_ctx* ctx) {
     const long long planes = (long long)p.B * p.Cin, nrows = planes * p.H;
     cudaError_t e = launch_rows_gemm<true>(x, reinterpret_cast<float*>(T), nrows, p.W, 2 * p.m2,
-                                           p.W, 1.f, p.tw_w, s);
+                                           p.W, 1.f, p.tw_w, p, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     if (e != cudaSuccess) return e;
     e = launch_cols_gemm<true>(T, X, 2 * p.m1, p.H, planes, p.m2, p.H, 2 * p.m1, p.H, p.m1,
-                               p.scale, p.tw_h, s);
+                               p.scale, p.tw_h, p, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
@@ -431,11 +436,11 @@ cudaError_t launch_inverse_dft(const fno_plan_s& p, const float2* Z, float* y, f
                                cudaStream_t s, fno_launch_ctx* ctx) {
     const long long planes = (long long)p.B * p.Cout, nrows = planes * p.H;
     cudaError_t e = launch_cols_gemm<false>(Z, T, p.H, 2 * p.m1, planes, p.m2, 2 * p.m1, p.H,
-                                            p.H, p.m1, 1.f, p.tw_h, s);
+                                            p.H, p.m1, 1.f, p.tw_h, p, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     if (e != cudaSuccess) return e;
     e = launch_rows_gemm<false>(reinterpret_cast<const float*>(T), y, nrows, 2 * p.m2, p.W, p.W,
-                                p.scale, p.tw_w, s);
+                                p.scale, p.tw_w, p, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
@@ -446,7 +451,7 @@ cudaError_t launch_forward_1d(const fno_plan_s& p, const float* x, float2* X, cu
                               fno_launch_ctx* ctx) {
     const long long nrows = (long long)p.B * p.Cin;
     cudaError_t e = launch_rows_gemm<true>(x, reinterpret_cast<float*>(X), nrows, p.W, 2 * p.m2,
-                                           p.W, p.scale, p.tw_w, s);
+                                           p.W, p.scale, p.tw_w, p, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
@@ -455,7 +460,7 @@ cudaError_t launch_inverse_1d(const fno_plan_s& p, const float2* Z, float* y, cu
                               fno_launch_ctx* ctx) {
     const long long nrows = (long long)p.B * p.Cout;
     cudaError_t e = launch_rows_gemm<false>(reinterpret_cast<const float*>(Z), y, nrows,
-                                            2 * p.m2, p.W, p.W, p.scale, p.tw_w, s);
+                                            2 * p.m2, p.W, p.W, p.scale, p.tw_w, p, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }

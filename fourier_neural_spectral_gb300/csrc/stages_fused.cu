@@ -43,7 +43,8 @@ template <int W, int R, int M1S = 0, int M2S = 0>
 __global__ void __launch_bounds__(kFT, (FusedCfg<W, R>::MinBlocks))
 fwd_fused_kernel(const float* __restrict__ x, float2* __restrict__ X, int H, int m1, int m2,
                  int P, float scale, const float2* __restrict__ tw_w,
-                 const float2* __restrict__ tw_h) {
+                 const float2* __restrict__ tw_h FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     using C = FusedCfg<W, R>;
     extern __shared__ float2 sm[];
     float2* scr = sm;
@@ -103,7 +104,8 @@ template <int W, int R, int M1S = 0, int M2S = 0, bool ZS = false>
 __global__ void __launch_bounds__(kFT, (FusedCfg<W, R>::MinBlocks))
 inv_fused_kernel(const float2* __restrict__ Z, float* __restrict__ y, int H, int m1, int m2,
                  int P, float scale, const float2* __restrict__ tw_w,
-                 const float2* __restrict__ tw_h, unsigned* __restrict__ err) {
+                 const float2* __restrict__ tw_h, unsigned* __restrict__ err FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     using C = FusedCfg<W, R>;
     extern __shared__ __align__(16) float2 sm[];
     float2* scr = sm;
@@ -176,7 +178,7 @@ __global__ void zero_kernel(float4* __restrict__ p, size_t n4) {
 
 template <int W, int R>
 cudaError_t set_attrs() {
-    const int bytes = (int)std::min<size_t>(fused_smem_bytes<W, R>(W / 2 + 1), 227 * 1024);
+    const int bytes = (int)std::min<size_t>(fused_smem_bytes<W, R>(W / 2 + 1), kMaxDynSmem);
     cudaError_t e = cudaFuncSetAttribute(fwd_fused_kernel<W, R>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess)
@@ -186,7 +188,7 @@ cudaError_t set_attrs() {
         e = cudaFuncSetAttribute(inv_fused_kernel<W, R, 0, 0, zs_compiled<W, R, 0>()>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if constexpr (has_static<W, R>()) {
-        const int sb = (int)std::min<size_t>(fused_smem_bytes<W, R>(W / 4), 227 * 1024);
+        const int sb = (int)std::min<size_t>(fused_smem_bytes<W, R>(W / 4), kMaxDynSmem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(fwd_fused_kernel<W, R, W / 4, W / 4>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, sb);
@@ -216,11 +218,12 @@ cudaError_t launch_fwd(const fno_plan_s& p, const float* x, float2* X, cudaStrea
     if constexpr (has_static<W, R>()) {
         if (p.m1 == W / 4 && p.m2 == W / 4) {
             return launch_pdl(fwd_fused_kernel<W, R, W / 4, W / 4>, grid, kFT, smem, s, x, X, p.H,
-                              p.m1, p.m2, p.P, p.scale, p.tw_w, p.tw_h);
+                              p.m1, p.m2, p.P, p.scale, p.tw_w, p.tw_h
+                              FNO_DBG_ARG1(X, 8ull * p.B * p.Cin * p.nm, p));
         }
     }
     return launch_pdl(fwd_fused_kernel<W, R>, grid, kFT, smem, s, x, X, p.H, p.m1, p.m2, p.P,
-                      p.scale, p.tw_w, p.tw_h);
+                      p.scale, p.tw_w, p.tw_h FNO_DBG_ARG1(X, 8ull * p.B * p.Cin * p.nm, p));
 }
 
 template <int W, int R, int M1S, int M2S>
@@ -229,9 +232,11 @@ cudaError_t launch_inv_zs(const fno_plan_s& p, const float2* Z, float* y, cudaSt
     const unsigned grid = (unsigned)((size_t)p.B * p.Cout * p.Pi);
     if (zs_compiled<W, R, M2S>() && fused_z_staged<W, R>(p.m1, p.m2))
         return launch_pdl(inv_fused_kernel<W, R, M1S, M2S, zs_compiled<W, R, M2S>()>, grid, kFT,
-                          smem, s, Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
+                          smem, s, Z, y, p.H, p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err
+                          FNO_DBG_ARG1(y, 4ull * p.B * p.Cout * p.H * p.W, p));
     return launch_pdl(inv_fused_kernel<W, R, M1S, M2S, false>, grid, kFT, smem, s, Z, y, p.H,
-                      p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err);
+                      p.m1, p.m2, p.Pi, p.scale, p.tw_w, p.tw_h, p.err
+                      FNO_DBG_ARG1(y, 4ull * p.B * p.Cout * p.H * p.W, p));
 }
 
 template <int W, int R>
@@ -306,7 +311,7 @@ bool fused_supported(int W, int H, int m1, int m2, int* R_fwd, int* R_inv) {
     const auto smem = [&](int R, bool fwd) {
         return W <= 256 ? fused_smem_bytes_any(W, R, m2) : big_smem_bytes_any(W, R, m2, fwd);
     };
-    if (smem(Rf, true) > 227 * 1024 || smem(Ri, false) > 227 * 1024) return false;
+    if (smem(Rf, true) > kMaxDynSmem || smem(Ri, false) > kMaxDynSmem) return false;
     *R_fwd = Rf;
     *R_inv = Ri;
     return true;

@@ -32,7 +32,8 @@ __device__ __forceinline__ int kept_row(int r, int H, int m1) { return r < m1 ? 
 // ---- a1: forward row transform of row pairs -------------------------------
 __global__ void __launch_bounds__(kThreads)
 fwd_rows_kernel(const float* __restrict__ x, float2* __restrict__ T, long long npairs, int W,
-                int m2, int S, const float2* __restrict__ tw) {
+                int m2, int S, const float2* __restrict__ tw FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     extern __shared__ float2 smem[];
     float2* a = smem;
     float2* b = smem + (size_t)S * W;
@@ -59,15 +60,16 @@ fwd_rows_kernel(const float* __restrict__ x, float2* __restrict__ T, long long n
         const float2 sum = make_float2(0.5f * (zk.x + zm.x), 0.5f * (zk.y - zm.y));
         // (Z[k] - conj Z[-k]) / (2i)
         const float2 dif = make_float2(0.5f * (zk.y + zm.y), -0.5f * (zk.x - zm.x));
-        T[(2 * pr) * m2 + k] = sum;
-        T[(2 * pr + 1) * m2 + k] = dif;
+        if (FNO_DBG_OK(&T[(2 * pr) * m2 + k], sizeof(float2))) T[(2 * pr) * m2 + k] = sum;
+        if (FNO_DBG_OK(&T[(2 * pr + 1) * m2 + k], sizeof(float2))) T[(2 * pr + 1) * m2 + k] = dif;
     }
 }
 
 // ---- a2: forward column transform, keep retained rows, scale ---------------
 __global__ void __launch_bounds__(kThreads)
 fwd_cols_kernel(const float2* __restrict__ T, float2* __restrict__ X, int H, int m1, int m2,
-                int S, float scale, const float2* __restrict__ tw) {
+                int S, float scale, const float2* __restrict__ tw FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     extern __shared__ float2 smem[];
     float2* a = smem;
     float2* b = smem + (size_t)S * H;
@@ -85,14 +87,16 @@ fwd_cols_kernel(const float2* __restrict__ T, float2* __restrict__ X, int H, int
     float2* Xp = X + plane * R * m2;
     for (int e = threadIdx.x; e < R * S; e += blockDim.x) {
         const int r = e / S, s = e - r * S;
-        if (s < ns) Xp[(long long)r * m2 + c0 + s] = cscale(res[s * H + kept_row(r, H, m1)], scale);
+        if (s < ns && FNO_DBG_OK(&Xp[(long long)r * m2 + c0 + s], sizeof(float2)))
+            Xp[(long long)r * m2 + c0 + s] = cscale(res[s * H + kept_row(r, H, m1)], scale);
     }
 }
 
 // ---- a4: inverse column transform of the zero-filled retained rows ---------
 __global__ void __launch_bounds__(kThreads)
 inv_cols_kernel(const float2* __restrict__ Z, float2* __restrict__ T, int H, int m1, int m2,
-                int S, const float2* __restrict__ tw) {
+                int S, const float2* __restrict__ tw FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     extern __shared__ float2 smem[];
     float2* a = smem;
     float2* b = smem + (size_t)S * H;
@@ -113,14 +117,16 @@ inv_cols_kernel(const float2* __restrict__ Z, float2* __restrict__ T, int H, int
     float2* Tp = T + plane * H * m2;
     for (int e = threadIdx.x; e < S * H; e += blockDim.x) {
         const int h = e / S, s = e - h * S;
-        if (s < ns) Tp[(long long)h * m2 + c0 + s] = res[s * H + h];
+        if (s < ns && FNO_DBG_OK(&Tp[(long long)h * m2 + c0 + s], sizeof(float2)))
+            Tp[(long long)h * m2 + c0 + s] = res[s * H + h];
     }
 }
 
 // ---- a5: complex-to-real row transform of row pairs -------------------------
 __global__ void __launch_bounds__(kThreads)
 inv_rows_kernel(const float2* __restrict__ T, float* __restrict__ y, long long npairs, int W,
-                int m2, int S, float scale, const float2* __restrict__ tw) {
+                int m2, int S, float scale, const float2* __restrict__ tw FNO_DBG_PARAM) {
+    FNO_DBG_BEGIN();
     extern __shared__ float2 smem[];
     float2* a = smem;
     float2* b = smem + (size_t)S * W;
@@ -158,8 +164,9 @@ inv_rows_kernel(const float2* __restrict__ T, float* __restrict__ y, long long n
         const long long pr = pair0 + s;
         if (pr >= npairs) continue;
         const float2 v = res[e];
-        y[(2 * pr) * W + n] = v.x * scale;
-        y[(2 * pr + 1) * W + n] = v.y * scale;
+        if (FNO_DBG_OK(&y[(2 * pr) * W + n], sizeof(float))) y[(2 * pr) * W + n] = v.x * scale;
+        if (FNO_DBG_OK(&y[(2 * pr + 1) * W + n], sizeof(float)))
+            y[(2 * pr + 1) * W + n] = v.y * scale;
     }
 }
 
@@ -190,7 +197,8 @@ cudaError_t launch_forward_modes(const fno_plan_s& p, const float* x, float2* X,
         const int S = seqs_for(p.W);
         const size_t smem = 2 * sizeof(float2) * (size_t)S * p.W;
         const long long grid = (npairs + S - 1) / S;
-        fwd_rows_kernel<<<(unsigned)grid, kThreads, smem, s>>>(x, T, npairs, p.W, p.m2, S, p.tw_w);
+        fwd_rows_kernel<<<(unsigned)grid, kThreads, smem, s>>>(
+            x, T, npairs, p.W, p.m2, S, p.tw_w FNO_DBG_ARG1(T, 16ull * npairs * p.m2, p));
         cudaError_t e = cudaGetLastError();
         if (e == cudaSuccess && ctx) e = ctx->mark(s);
         if (e != cudaSuccess) return e;
@@ -199,7 +207,8 @@ cudaError_t launch_forward_modes(const fno_plan_s& p, const float* x, float2* X,
         const int S = std::min(seqs_for(p.H), p.m2);
         const size_t smem = 2 * sizeof(float2) * (size_t)S * p.H;
         dim3 grid((unsigned)(p.B * p.Cin), (p.m2 + S - 1) / S);
-        fwd_cols_kernel<<<grid, kThreads, smem, s>>>(T, X, p.H, p.m1, p.m2, S, p.scale, p.tw_h);
+        fwd_cols_kernel<<<grid, kThreads, smem, s>>>(
+            T, X, p.H, p.m1, p.m2, S, p.scale, p.tw_h FNO_DBG_ARG1(X, 8ull * p.B * p.Cin * p.nm, p));
         cudaError_t e = cudaGetLastError();
         if (e == cudaSuccess && ctx) e = ctx->mark(s);
         if (e != cudaSuccess) return e;
@@ -214,7 +223,8 @@ cudaError_t launch_inverse_modes(const fno_plan_s& p, const float2* Z, float* y,
         const int S = std::min(seqs_for(p.H), p.m2);
         const size_t smem = 2 * sizeof(float2) * (size_t)S * p.H;
         dim3 grid((unsigned)(p.B * p.Cout), (p.m2 + S - 1) / S);
-        inv_cols_kernel<<<grid, kThreads, smem, s>>>(Z, T, p.H, p.m1, p.m2, S, p.tw_h);
+        inv_cols_kernel<<<grid, kThreads, smem, s>>>(
+            Z, T, p.H, p.m1, p.m2, S, p.tw_h FNO_DBG_ARG1(T, 8ull * p.B * p.Cout * p.H * p.m2, p));
         cudaError_t e = cudaGetLastError();
         if (e == cudaSuccess && ctx) e = ctx->mark(s);
         if (e != cudaSuccess) return e;
@@ -224,8 +234,8 @@ cudaError_t launch_inverse_modes(const fno_plan_s& p, const float2* Z, float* y,
         const int S = seqs_for(p.W);
         const size_t smem = 2 * sizeof(float2) * (size_t)S * p.W;
         const long long grid = (npairs + S - 1) / S;
-        inv_rows_kernel<<<(unsigned)grid, kThreads, smem, s>>>(T, y, npairs, p.W, p.m2, S, p.scale,
-                                                               p.tw_w);
+        inv_rows_kernel<<<(unsigned)grid, kThreads, smem, s>>>(
+            T, y, npairs, p.W, p.m2, S, p.scale, p.tw_w FNO_DBG_ARG1(y, 8ull * npairs * p.W, p));
         cudaError_t e = cudaGetLastError();
         if (e == cudaSuccess && ctx) e = ctx->mark(s);
         if (e != cudaSuccess) return e;

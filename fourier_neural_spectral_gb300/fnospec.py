@@ -14,7 +14,11 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libfnospec.so")
+# FNO_DEBUG_BOUNDS=1 selects the range-checked build (python -m
+# fourier_neural_spectral_gb300.build --debug): every global store of the main
+# kernels is checked against its launch's output ranges.
+LIB_PATH = os.path.join(_PKG, "libfnospec_debug.so" if os.environ.get("FNO_DEBUG_BOUNDS") == "1"
+                        else "libfnospec.so")
 
 FNO_OK = 0
 FNO_ERR_INVALID_ARG = 1
@@ -39,7 +43,7 @@ EXPORTS = (
     "fno_release_cache", "fno_forward_modes", "fno_mix_modes", "fno_inverse_modes",
     "fno_get_device_status", "fno_spectral_conv2d_noalloc", "fno_plan_backward",
     "fno_block_epilogue", "fno_block_execute", "fno_plan_create_1d",
-    "fno_plan_debug_force_timeout", "fno_plan_set_single_launch",
+    "fno_plan_debug_force_timeout", "fno_plan_set_single_launch", "fno_plan_debug_bounds_margin",
 )
 
 
@@ -72,6 +76,7 @@ def load_library(path: str = LIB_PATH):
             "fno_plan_create_1d": (st, [ctypes.POINTER(vp), i, i, i, i, i, i]),
             "fno_plan_debug_force_timeout": (st, [vp, i]),
             "fno_plan_set_single_launch": (st, [vp, i]),
+            "fno_plan_debug_bounds_margin": (st, [vp, sz]),
             "fno_plan_workspace_size": (st, [vp, ctypes.POINTER(sz)]),
             "fno_plan_launch_count": (st, [vp, ctypes.POINTER(i)]),
             "fno_plan_describe": (st, [vp, ctypes.c_char_p, sz]),

@@ -276,6 +276,19 @@ fno_status_t fno_spectral_conv2d_noalloc(const float* x, const void* w, float* y
  * Calls that use the same plan must not overlap on the GPU. */
 fno_status_t fno_plan_set_single_launch(fno_plan_t plan, int enable);
 
+/* Range-checked builds (libfnospec_debug.so, compiled with FNO_DEBUG): every
+ * global store of the kernels on the execute, stage, backward and single-launch
+ * paths is checked against the output ranges of its launch; a store outside
+ * them is skipped (nothing is written, nothing traps) and bit 0 of the plan's
+ * device error word is set, so fno_get_device_status returns FNO_ERR_DEVICE.
+ * This test hook shortens the first output range of every launch of the plan
+ * (and of its backward) by `bytes`, so that the last outputs count as out of
+ * range without any access leaving its tensor.  bytes = 0 restores the true
+ * ranges.  Returns FNO_ERR_UNSUPPORTED in release builds (no checks compiled),
+ * FNO_ERR_INVALID_ARG for a NULL plan.  Host-only.  A stand-in for a memory
+ * checker where none can run; the pages have no counterpart. */
+fno_status_t fno_plan_debug_bounds_margin(fno_plan_t plan, size_t bytes);
+
 /* Synchronise stream s, read and clear the plan's device error word.  Returns
  * FNO_OK, FNO_ERR_TIMEOUT or FNO_ERR_DEVICE (or FNO_ERR_CUDA if the copy fails).
  * This is the stage-by-stage fault check of the FFT operator-optimisation page,
