@@ -383,6 +383,8 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
         p->shares_tables = true;
         p->tw_h = parent->tw_h;
         p->tw_w = parent->tw_w;
+        p->g_irows = parent->g_irows;
+        p->g_frows = parent->g_frows;
         p->err = parent->err;
         return p;
     }
@@ -396,6 +398,25 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
     if (e == cudaSuccess) e = cudaMemcpy(p->tw_h, th.data(), sizeof(float2) * H, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(p->tw_w, tw.data(), sizeof(float2) * W, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(p->err, 0, 2 * sizeof(unsigned));
+    // the direct-DFT inverse rows stream their twiddle tiles from the plan
+    if (e == cudaSuccess && p->path == 0 && (dims == 1 || dft_path(H, W))) {
+        const std::vector<float> g = dft_irows_table(W, m2, (double)p->scale);
+        if (!g.empty()) {
+            e = cudaMalloc(&p->g_irows, sizeof(float) * g.size());
+            if (e == cudaSuccess)
+                e = cudaMemcpy(p->g_irows, g.data(), sizeof(float) * g.size(),
+                               cudaMemcpyHostToDevice);
+        }
+        // the forward rows carry the 1D layer's 1/sqrt(L); in 2D the columns
+        // apply the scale
+        const std::vector<float> f = dft_frows_table(W, m2, dims == 1 ? (double)p->scale : 1.0);
+        if (e == cudaSuccess && !f.empty()) {
+            e = cudaMalloc(&p->g_frows, sizeof(float) * f.size());
+            if (e == cudaSuccess)
+                e = cudaMemcpy(p->g_frows, f.data(), sizeof(float) * f.size(),
+                               cudaMemcpyHostToDevice);
+        }
+    }
     if (e != cudaSuccess) {
         fno_plan_destroy(p);
         return nullptr;
@@ -453,6 +474,8 @@ fno_status_t fno_plan_destroy(fno_plan_t p) {
     if (!p->shares_tables) {
         if (p->tw_h) cudaFree(p->tw_h);
         if (p->tw_w) cudaFree(p->tw_w);
+        if (p->g_irows) cudaFree(p->g_irows);
+        if (p->g_frows) cudaFree(p->g_frows);
         if (p->err) cudaFree(p->err);
         if (p->gbar) cudaFree(p->gbar);
     }

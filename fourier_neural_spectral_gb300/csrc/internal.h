@@ -2,6 +2,8 @@
 // libfnospec.  Not part of the public ABI (that is include/fnospec.h).
 #pragma once
 
+#include <vector>
+
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -92,6 +94,8 @@ struct fno_plan_s {
     float scale;            // 1/sqrt(H*W), rounded once from double
     float2* tw_h;           // e^{+2 pi i j / H}, j in [0, H)
     float2* tw_w;           // e^{+2 pi i j / W}, j in [0, W)
+    float* g_irows;         // direct-DFT inverse rows: twiddle tiles (dft_irows_table), or null
+    float* g_frows;         // direct-DFT forward rows: twiddle tiles (dft_frows_table), or null
     unsigned* err;          // device error word
     unsigned long long* gbar;  // grid-barrier counter of the single-launch layer
     int single_launch;      // execute runs the whole layer as one launch
@@ -196,6 +200,13 @@ cudaError_t launch_layer_persistent(const fno_plan_s& p, const float* x, const f
 // Direct-DFT transforms for H or W not a power of two (stages_dft.cu); the
 // shape-generic launchers below route such shapes there.
 bool dft_path(int H, int W);
+// Twiddle tiles of the direct-DFT inverse row step for rows of W points and m2
+// retained columns (empty when that step does not use them), in the layout
+// dft_irows_kernel streams: [pass][4 shifts][2*m2][64] floats.
+std::vector<float> dft_irows_table(int W, int m2, double scale);
+// The same for the forward row step ([pass][4 shifts][64][NP] floats, NP = 2*m2
+// rounded up to 8, 16, 24 or 32; empty above 32).
+std::vector<float> dft_frows_table(int W, int m2, double scale);
 cudaError_t stages_dft_init();
 cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, float2* T,
                                cudaStream_t s, fno_launch_ctx* ctx);

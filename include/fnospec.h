@@ -304,9 +304,10 @@ fno_status_t fno_get_device_status(fno_plan_t plan, cudaStream_t s);
  * tensor-core work finish, frees what it holds and returns, so the context
  * stays usable; outputs of such calls are void and the next
  * fno_get_device_status returns FNO_ERR_TIMEOUT.  Kernels without waits
- * (the shape-generic and direct-DFT transforms, the short-row forward) are not
- * affected.  enable = 0 restores normal operation.  Host-synchronous: it
- * synchronises the device before it writes the flag, so call it between calls,
+ * (the shape-generic transforms, the direct-DFT steps other than the inverse
+ * rows, the short-row forward) are not affected.  enable = 0 restores normal
+ * operation.  Host-synchronous: it synchronises the device before it writes
+ * the flag, so call it between calls,
  * never during stream capture.  Returns FNO_ERR_INVALID_ARG for a NULL plan or
  * another current device, FNO_ERR_CUDA if the device copy fails.  A test hook
  * of this library: no page defines it. */

@@ -30,6 +30,7 @@ SHAPES_1D = [
     (3, 5, 7, 512, 40),       # FFT rows (L >= 512, m <= 64), odd sequence counts 15 / 21
     (1, 3, 2, 2048, 64),      # FFT rows, 64 modes, 3 / 2 sequences
     (1, 2, 3, 256, 100),      # direct DFTs with K split over CTAs both ways (2m = 200)
+    (48, 832, 2, 1000, 12),   # 39,936 sequences: residue-class forward rows, streamed tiles
 ]
 
 

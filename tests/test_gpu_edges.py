@@ -67,6 +67,28 @@ def test_edge_shapes_match_oracle(cuda_lib, shape):
     assert_fp32_close(y, ref, str(shape))
 
 
+# Direct-DFT grids whose rows (W >= ~200) take the pass kernels with streamed
+# twiddle tiles, with enough rows (B * Cin * H >= 38,912) for the residue-class
+# forward kernel: 32, 8 (W = 3 mod 4: all four row alignments) and 24 outputs
+# per row.
+MANY_ROW_SHAPES = [
+    (8, 16, 4, 333, 333, 8, 16),
+    (4, 32, 2, 305, 307, 6, 3),
+    (4, 24, 4, 421, 421, 12, 12),
+]
+
+
+@pytest.mark.parametrize("shape", MANY_ROW_SHAPES)
+def test_direct_dft_many_rows_match_oracle(cuda_lib, shape):
+    B, Cin, Cout, H, W, m1, m2 = shape
+    rng = np.random.default_rng(sum(shape) + 5)
+    x, w = rand_layer_inputs(rng, B, Cin, Cout, H, W, m1, m2)
+    y, plan = run_layer(x, w, m1, m2)
+    assert "direct-dft" in plan.description
+    ref = oracle.spectral_conv2d(x, f32pairs_to_cplx(w), m1, m2)
+    assert_fp32_close(y, ref, str(shape))
+
+
 @pytest.mark.parametrize("H,W", [(16, 16), (8, 64), (128, 32)])
 def test_identity_weights_full_modes_return_input(cuda_lib, H, W):
     C, m1, m2 = 3, H // 2, W // 2 + 1

@@ -10,7 +10,8 @@ with the hook cleared again matches the oracle.  The cases cover every kernel
 family that waits on an mbarrier: the 32-mode contraction (TMA ring with a
 producer warp), the inverse transforms that stage Z by one bulk copy (short and
 long rows), the long-row forward that stages row pairs, the tcgen05 contraction
-(TMEM accumulators), the block epilogue and the backward.
+(TMEM accumulators), the direct-DFT inverse rows (bulk-copied twiddle tiles),
+the block epilogue and the backward.
 """
 import numpy as np
 import pytest
@@ -27,6 +28,7 @@ CASES = [
     ((1, 8, 8, 512, 512, 16, 16), "fp32", "fwd_fused"),     # long rows: staged pairs, staged Z
     ((2, 32, 32, 64, 64, 16, 16), "tf32", "mix_tcm"),       # tcgen05, weights in TMEM
     ((32, 32, 32, 16, 16, 4, 4), "tf32", "mix_tc_"),        # tcgen05, operands in smem
+    ((2, 8, 8, 30, 50, 6, 9), "fp32", "dft_irows"),          # direct DFT: streamed twiddle tiles
 ]
 
 
