@@ -385,6 +385,7 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
         p->tw_w = parent->tw_w;
         p->g_irows = parent->g_irows;
         p->g_frows = parent->g_frows;
+        p->g_cols = parent->g_cols;
         p->err = parent->err;
         return p;
     }
@@ -414,6 +415,14 @@ fno_plan_s* plan_new(int dims, int B, int Cin, int Cout, int H, int W, int m1, i
             e = cudaMalloc(&p->g_frows, sizeof(float) * f.size());
             if (e == cudaSuccess)
                 e = cudaMemcpy(p->g_frows, f.data(), sizeof(float) * f.size(),
+                               cudaMemcpyHostToDevice);
+        }
+        // the column steps of the 2D direct-DFT path
+        if (e == cudaSuccess && dims == 2) {
+            const std::vector<float2> c = dft_cols_table(H, m1);
+            e = cudaMalloc(&p->g_cols, sizeof(float2) * c.size());
+            if (e == cudaSuccess)
+                e = cudaMemcpy(p->g_cols, c.data(), sizeof(float2) * c.size(),
                                cudaMemcpyHostToDevice);
         }
     }
@@ -476,6 +485,7 @@ fno_status_t fno_plan_destroy(fno_plan_t p) {
         if (p->tw_w) cudaFree(p->tw_w);
         if (p->g_irows) cudaFree(p->g_irows);
         if (p->g_frows) cudaFree(p->g_frows);
+        if (p->g_cols) cudaFree(p->g_cols);
         if (p->err) cudaFree(p->err);
         if (p->gbar) cudaFree(p->gbar);
     }

@@ -96,6 +96,7 @@ struct fno_plan_s {
     float2* tw_w;           // e^{+2 pi i j / W}, j in [0, W)
     float* g_irows;         // direct-DFT inverse rows: twiddle tiles (dft_irows_table), or null
     float* g_frows;         // direct-DFT forward rows: twiddle tiles (dft_frows_table), or null
+    float2* g_cols;         // direct-DFT column steps: twiddle matrices (dft_cols_table), or null
     unsigned* err;          // device error word
     unsigned long long* gbar;  // grid-barrier counter of the single-launch layer
     int single_launch;      // execute runs the whole layer as one launch
@@ -207,6 +208,10 @@ std::vector<float> dft_irows_table(int W, int m2, double scale);
 // The same for the forward row step ([pass][4 shifts][64][NP] floats, NP = 2*m2
 // rounded up to 8, 16, 24 or 32; empty above 32).
 std::vector<float> dft_frows_table(int W, int m2, double scale);
+// The column steps' twiddle matrices for columns of H points and 2*m1 retained
+// rows k1(r): the forward's At[h][r] = e^{-2 pi i k1(r) h / H} (H x 2m1) followed
+// by the inverse's At[r][h] = e^{+2 pi i k1(r) h / H} (2m1 x H).
+std::vector<float2> dft_cols_table(int H, int m1);
 cudaError_t stages_dft_init();
 cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, float2* T,
                                cudaStream_t s, fno_launch_ctx* ctx);

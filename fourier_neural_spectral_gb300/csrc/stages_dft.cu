@@ -539,12 +539,18 @@ dft_frows_kernel(const float* __restrict__ x, float* __restrict__ C, long long M
 //   forward  X_q[r][k2] = s * sum_h F[r][h] T_q[h][k2],  F[r][h] = e^{-2 pi i k1(r) h / H},
 //   inverse  T_q[h][k2] = sum_r G[h][r] Z_q[r][k2],      G[h][r] = e^{+2 pi i k1(r) h / H},
 // i.e. C[m][c] = alpha * sum_k A[m][k] B[k][c], with B[k][(q, k2)] at
-// (q*KB + k)*m2 + k2 and C[m][(q, k2)] at (q*MC + m)*m2 + k2.  A is formed per K
-// chunk from the table e^{+2 pi i j / H} (forward: index kept incrementally).
+// (q*KB + k)*m2 + k2 and C[m][(q, k2)] at (q*MC + m)*m2 + k2.  A comes from a
+// plan table stored as At[k][m] (dft_cols_table: forward At[h][r] =
+// e^{-2 pi i k1(r) h / H}, inverse At[r][h] = e^{+2 pi i k1(r) h / H}), read
+// per K chunk (consecutive lanes, consecutive m); without one (the
+// allocation-free entry point) it is formed from the table e^{+2 pi i j / H} at
+// the exact index (k1 * h) mod H.
 // CTA: 128 threads, 32 rows x 32 complex columns; each thread 4 rows x 2
 // columns (columns tx and tx + 16, so that 16 lanes store 128 contiguous
 // bytes); per K step two float4 of A and two float2 of B feed 32 fused
-// multiply-adds.  Chunks of 16 are double buffered.
+// multiply-adds.  Chunks of 16 are double buffered.  With few tiles the K
+// range is split over gridDim.y CTAs whose partial sums are added into C,
+// which the launcher has zeroed.
 constexpr int kCT = 128;   // threads
 constexpr int kCBK = 16;   // K chunk
 constexpr int kCBM = 32;   // rows per CTA
@@ -554,7 +560,8 @@ template <bool FWD>
 __global__ void __launch_bounds__(kCT)
 dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst, int M, int K,
                      long long ncols, int m2, int KB, int MC, int H, int m1, float alpha,
-                     const float2* __restrict__ tw_h FNO_DBG_PARAM) {
+                     const float2* __restrict__ At, const float2* __restrict__ tw_h,
+                     int kper FNO_DBG_PARAM) {
     FNO_DBG_BEGIN();
     __shared__ __align__(16) float2 As[2][kCBK][kCBM];
     __shared__ __align__(16) float2 Bs[2][kCBK][kCBN];
@@ -573,46 +580,34 @@ dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst,
     const float2* Bcol = Bsrc + (size_t)bq * KB * m2 + bk2;
     const int am = m0 + lc;
     const bool avalid = am < M;
-    const auto k1_of = [H, m1](int r) { return r < m1 ? r : H - 2 * m1 + r; };
-    // forward: A[m][k] = conj(tab[(k1(m) * k) mod H]), k1 fixed per thread
-    const int ak1 = FWD && avalid ? k1_of(am) : 0;
-    int abase = FWD ? (int)(((long long)ak1 * lk) % H) : 0;
-    const int astep = FWD ? (int)(((long long)ak1 * 4) % H) : 0;
-    const int aadv = FWD ? (int)(((long long)ak1 * kCBK) % H) : 0;
+    const int kbeg = (int)blockIdx.y * kper, kend = min(K, kbeg + kper);
 
     float2 rb[4];
+    float2 ra[4];
     const auto load_b = [&](int k0) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int k = k0 + lk + 4 * i;
-            rb[i] = bvalid && k < K ? __ldg(&Bcol[(size_t)k * m2]) : make_float2(0.f, 0.f);
-        }
-    };
-    const auto store_chunk = [&](int buf, int k0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) Bs[buf][lk + 4 * i][lc] = rb[i];
-        int idx = abase;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int k = k0 + lk + 4 * i;
+            rb[i] = bvalid && k < kend ? __ldg(&Bcol[(size_t)k * m2]) : make_float2(0.f, 0.f);
             float2 a = make_float2(0.f, 0.f);
-            if (avalid && k < K) {
-                if (FWD) {
-                    a = __ldg(&tw_h[idx]);
-                    a.y = -a.y;
+            if (avalid && k < kend) {
+                if (At) {
+                    a = __ldg(&At[(size_t)k * M + am]);
                 } else {
-                    a = __ldg(&tw_h[(int)(((long long)k1_of(k) * am) % H)]);
+                    const int r = FWD ? am : k, h = FWD ? k : am;
+                    const int k1 = r < m1 ? r : H - 2 * m1 + r;
+                    a = __ldg(&tw_h[(int)(((long long)k1 * h) % H)]);
+                    if (FWD) a.y = -a.y;
                 }
             }
-            As[buf][lk + 4 * i][lc] = a;
-            if (FWD) {
-                idx += astep;
-                if (idx >= H) idx -= H;
-            }
+            ra[i] = a;
         }
-        if (FWD) {
-            abase += aadv;
-            if (abase >= H) abase -= H;
+    };
+    const auto store_chunk = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            Bs[buf][lk + 4 * i][lc] = rb[i];
+            As[buf][lk + 4 * i][lc] = ra[i];
         }
     };
 
@@ -620,12 +615,12 @@ dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst,
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
 
-    load_b(0);
-    store_chunk(0, 0);
+    load_b(kbeg);
+    store_chunk(0);
     __syncthreads();
     int buf = 0;
-    for (int k0 = 0; k0 < K; k0 += kCBK) {
-        const bool more = k0 + kCBK < K;
+    for (int k0 = kbeg; k0 < kend; k0 += kCBK) {
+        const bool more = k0 + kCBK < kend;
         if (more) load_b(k0 + kCBK);
 #pragma unroll
         for (int kk = 0; kk < kCBK; ++kk) {
@@ -639,7 +634,7 @@ dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst,
 #pragma unroll
                 for (int j = 0; j < 2; ++j) cmac(acc[i][j], av[i], bv[j]);
         }
-        if (more) store_chunk(buf ^ 1, k0 + kCBK);
+        if (more) store_chunk(buf ^ 1);
         __syncthreads();
         buf ^= 1;
     }
@@ -652,8 +647,11 @@ dft_cols_gemm_kernel(const float2* __restrict__ Bsrc, float2* __restrict__ Cdst,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int m = m0 + ty * 4 + i;
-            if (m < M && FNO_DBG_OK(&Cdst[((size_t)q * MC + m) * m2 + k2], sizeof(float2)))
-                Cdst[((size_t)q * MC + m) * m2 + k2] = cscale(acc[i][j], alpha);
+            float2* dst = &Cdst[((size_t)q * MC + m) * m2 + k2];
+            if (m < M && FNO_DBG_OK(dst, sizeof(float2))) {
+                if (gridDim.y == 1) *dst = cscale(acc[i][j], alpha);
+                else atomicAdd(dst, cscale(acc[i][j], alpha));
+            }
         }
     }
 }
@@ -757,12 +755,29 @@ cudaError_t launch_rows_gemm(const float* A, float* C, long long M, int K, int N
 
 template <bool FWD>
 cudaError_t launch_cols_gemm(const float2* B, float2* C, int M, int K, long long planes, int m2,
-                             int KB, int MC, int H, int m1, float alpha, const float2* tw_h,
-                             const fno_plan_s& p, cudaStream_t s) {
+                             int KB, int MC, float alpha, const float2* At, const fno_plan_s& p,
+                             cudaStream_t s) {
+    // without the plan's matrices (the allocation-free entry point) the
+    // kernel forms A from the twiddle table
     const long long ncols = planes * m2;
-    const long long grid = (long long)((M + kCBM - 1) / kCBM) * ((ncols + kCBN - 1) / kCBN);
-    dft_cols_gemm_kernel<FWD><<<(unsigned)grid, kCT, 0, s>>>(
-        B, C, M, K, ncols, m2, KB, MC, H, m1, alpha, tw_h
+    const long long tiles = (long long)((M + kCBM - 1) / kCBM) * ((ncols + kCBN - 1) / kCBN);
+    // with fewer than eight 4-warp CTAs per SM the K range is split (chunks of
+    // at least 64) and the partial sums are added into the zeroed C; their
+    // order of addition varies from run to run.  421x421 B16 C64 m = 12
+    // (forward: 384 tiles, K = 421): 53 -> 50 us with the memset
+    int ksplit = 1;
+    constexpr long long kWantCols = 8 * 152;
+    if (tiles < kWantCols && K >= 2 * 64)
+        ksplit = (int)std::min<long long>((kWantCols + tiles - 1) / tiles, K / 64);
+    int kper = (K + ksplit - 1) / ksplit;
+    kper = (kper + kCBK - 1) / kCBK * kCBK;
+    ksplit = (K + kper - 1) / kper;
+    if (ksplit > 1) {
+        cudaError_t e = cudaMemsetAsync(C, 0, 8ull * planes * MC * m2, s);
+        if (e != cudaSuccess) return e;
+    }
+    dft_cols_gemm_kernel<FWD><<<dim3((unsigned)tiles, (unsigned)ksplit), kCT, 0, s>>>(
+        B, C, M, K, ncols, m2, KB, MC, p.H, p.m1, alpha, At, p.tw_h, kper
         FNO_DBG_ARG1(C, 8ull * planes * MC * m2, p));
     return cudaGetLastError();
 }
@@ -771,6 +786,23 @@ cudaError_t launch_cols_gemm(const float2* B, float2* C, int M, int K, long long
 }  // namespace fno
 
 using namespace fno;
+
+std::vector<float2> dft_cols_table(int H, int m1) {
+    const int R2 = 2 * m1;
+    std::vector<float2> t(2ull * R2 * H);
+    const double two_pi = 6.283185307179586476925286766559005768;
+    for (int r = 0; r < R2; ++r) {
+        const int k1 = r < m1 ? r : H - R2 + r;
+        for (int h = 0; h < H; ++h) {
+            const long long idx = ((long long)k1 * h) % H;
+            const double a = two_pi * (double)idx / (double)H;
+            const float c = (float)std::cos(a), sn = (float)std::sin(a);
+            t[(size_t)h * R2 + r] = make_float2(c, -sn);                 // forward At[h][r]
+            t[(size_t)R2 * H + (size_t)r * H + h] = make_float2(c, sn);  // inverse At[r][h]
+        }
+    }
+    return t;
+}
 
 std::vector<float> dft_frows_table(int W, int m2, double scale) {
     const int N = 2 * m2, NP = frows_np(N);
@@ -847,8 +879,8 @@ cudaError_t launch_forward_dft(const fno_plan_s& p, const float* x, float2* X, f
                                            p.W, 1.f, p.tw_w, p, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     if (e != cudaSuccess) return e;
-    e = launch_cols_gemm<true>(T, X, 2 * p.m1, p.H, planes, p.m2, p.H, 2 * p.m1, p.H, p.m1,
-                               p.scale, p.tw_h, p, s);
+    e = launch_cols_gemm<true>(T, X, 2 * p.m1, p.H, planes, p.m2, p.H, 2 * p.m1, p.scale,
+                               p.g_cols, p, s);  // g_cols may be null (see the launcher)
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     return e;
 }
@@ -857,7 +889,8 @@ cudaError_t launch_inverse_dft(const fno_plan_s& p, const float2* Z, float* y, f
                                cudaStream_t s, fno_launch_ctx* ctx) {
     const long long planes = (long long)p.B * p.Cout, nrows = planes * p.H;
     cudaError_t e = launch_cols_gemm<false>(Z, T, p.H, 2 * p.m1, planes, p.m2, 2 * p.m1, p.H,
-                                            p.H, p.m1, 1.f, p.tw_h, p, s);
+                                            1.f, p.g_cols ? p.g_cols + 2ull * p.m1 * p.H : nullptr,
+                                            p, s);
     if (e == cudaSuccess && ctx) e = ctx->mark(s);
     if (e != cudaSuccess) return e;
     e = launch_rows_gemm<false>(reinterpret_cast<const float*>(T), y, nrows, 2 * p.m2, p.W, p.W,
