@@ -224,6 +224,10 @@ bool block_supported(int Cin) { return Cin >= 1 && Cin <= kMaxCin; }
 cudaError_t launch_block_epilogue(const fno_plan_s& p, const float* x, const float* w_pw,
                                   const float* bias, int act, float* y, bool after_own_inverse,
                                   cudaStream_t s) {
+    // up to 64 output channels the pointwise branch runs on the tensor cores
+    // (block_tc.cu); wider blocks keep this fp32 kernel
+    if (block_tc_supported(p.Cin, p.Cout))
+        return launch_block_tc(p, x, w_pw, bias, act, y, after_own_inverse, s);
     const int P = p.H * p.W;
     CUtensorMap mx;
     if (!encode_x_map(&mx, x, p.B, p.Cin, P)) return cudaErrorInvalidValue;

@@ -225,6 +225,7 @@ cudaError_t init_device() {
     if (e == cudaSuccess) e = mix_tma_init();
     if (e == cudaSuccess) e = mix_wide_init();
     if (e == cudaSuccess) e = block_init();
+    if (e == cudaSuccess) e = block_tc_init();
     if (e == cudaSuccess) e = mix_tc_init();
     if (e == cudaSuccess) e = mix_tcm_init();
     if (e == cudaSuccess) e = layer_persistent_init();

@@ -167,6 +167,11 @@ cudaError_t launch_wgrad_wide(const fno_plan_s& p, const float2* X, const float2
 // FNO block epilogue (block.cu).
 cudaError_t block_init();
 bool block_supported(int Cin);
+cudaError_t block_tc_init();
+bool block_tc_supported(int Cin, int Cout);
+cudaError_t launch_block_tc(const fno_plan_s& p, const float* x, const float* w_pw,
+                            const float* bias, int act, float* y, bool after_own_inverse,
+                            cudaStream_t s);
 cudaError_t launch_block_epilogue(const fno_plan_s& p, const float* x, const float* w_pw,
                                   const float* bias, int act, float* y, bool after_own_inverse,
                                   cudaStream_t s);

@@ -103,6 +103,17 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8]) {
     for (int i = 0; i < 8; ++i) r[i] = __uint_as_float(u[i]);
 }
 
+// Warp-wide: lane l reads 4 consecutive 32-bit columns of TMEM lane taddr.lane + l.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&r)[4]) {
+    uint32_t u[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = __uint_as_float(u[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

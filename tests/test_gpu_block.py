@@ -3,7 +3,8 @@
 fno_block_execute = fno_plan_execute then fno_block_epilogue (in place over y);
 compared element by element with oracle.block in double, on shapes covering
 ragged pixel tiles (P < 128), ragged channel chunks (Cin not a multiple of 32),
-two output-channel blocks (Cout > 64), no bias and no activation.
+two output-channel blocks (Cout > 64, the fp32 kernel), the tensor-core pointwise
+branch (Cout <= 64) with several units per CTA, no bias and no activation.
 """
 import numpy as np
 import pytest
@@ -21,6 +22,10 @@ BLOCK_CASES = [
     ((1, 3, 70, 32, 32, 8, 8), "gelu", False),    # two output blocks, one short chunk
     ((1, 100, 5, 8, 8, 2, 3), "none", True),      # four channel chunks, P = 64 < 128
     ((2, 33, 9, 16, 64, 8, 33), "none", False),   # Nyquist column, ragged channels
+    # tensor-core pointwise branch (Cout <= 64): several units per CTA, so the
+    # double-buffered accumulators and y tiles are reused many times
+    ((4, 64, 64, 128, 128, 32, 32), "gelu", True),
+    ((2, 32, 32, 256, 256, 16, 16), "none", True),
 ]
 
 
