@@ -143,10 +143,15 @@ KERNEL_SOURCES = {
     "layer_persistent": (r"\blayer_persistent_kernel\b",
                          ["layer_persistent.cu", "fused_rows.cuh", "fused_columns.cuh",
                           "fft_reg.cuh", "tma.cuh"] + _COMMON),
-    "dft_rows": (r"\bdft_rows_gemm_kernel<[0-9]+, [0-9]+, true", ["stages_dft.cu"] + _COMMON),
-    "dft_irows": (r"\bdft_rows_gemm_kernel<[0-9]+, [0-9]+, false", ["stages_dft.cu"] + _COMMON),
-    "dft_cols": (r"\bdft_cols_gemm_kernel<true>", ["stages_dft.cu"] + _COMMON),
-    "dft_icols": (r"\bdft_cols_gemm_kernel<false>", ["stages_dft.cu"] + _COMMON),
+    # ncu prints a bool template argument as 1 / 0
+    "dft_rows": (r"\b(dft_rows_gemm_kernel<[0-9]+, [0-9]+, (true|1),|dft_frows_kernel<)",
+                 ["stages_dft.cu", "tma.cuh"] + _COMMON),
+    "dft_irows": (r"\b(dft_rows_gemm_kernel<[0-9]+, [0-9]+, (false|0),|dft_irows_kernel\b)",
+                  ["stages_dft.cu", "tma.cuh"] + _COMMON),
+    "dft_cols": (r"\bdft_cols_gemm_kernel<(true|1)>", ["stages_dft.cu"] + _COMMON),
+    "dft_icols": (r"\bdft_cols_gemm_kernel<(false|0)>", ["stages_dft.cu"] + _COMMON),
+    "block_tc": (r"\bblock_tc_kernel<", ["block_tc.cu", "tcgen05.cuh", "tma.cuh"] + _COMMON),
+    "block_fp32": (r"\bblock_epilogue_kernel<", ["block.cu", "tma.cuh"] + _COMMON),
 }
 
 

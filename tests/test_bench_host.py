@@ -91,6 +91,11 @@ def test_kernel_patterns_pick_one_name_each():
         "inv_fused", "mix_wide_kernel<16, 0>": "mix_wide", "layer_persistent_kernel<64, 16, 16>":
         "layer_persistent", "dft_rows_gemm_kernel<64, 4, true, true>": "dft_rows",
         "dft_rows_gemm_kernel<64, 2, false, false>": "dft_irows",
+        "dft_frows_kernel<24>": "dft_rows", "dft_irows_kernel": "dft_irows",
+        "dft_cols_gemm_kernel<true>": "dft_cols", "dft_cols_gemm_kernel<false>": "dft_icols",
+        "dft_cols_gemm_kernel<1>": "dft_cols", "dft_cols_gemm_kernel<0>": "dft_icols",
+        "dft_rows_gemm_kernel<32, 4, 1, 1>": "dft_rows", "dft_rows_gemm_kernel<64, 2, 0, 0>": "dft_irows",
+        "block_tc_kernel<64>": "block_tc", "block_epilogue_kernel<8>": "block_fp32",
     }
     for name, want in demangled.items():
         hits = [k for k, (rx, _) in bench.KERNEL_SOURCES.items()
