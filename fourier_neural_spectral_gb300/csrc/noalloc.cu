@@ -48,7 +48,10 @@ bool reachable(const void* p) {
 // no status query covers this entry point.  Its stages must therefore stay on
 // kernels that cannot fail on the device (the shape-generic and direct-DFT
 // transforms and the per-thread contraction have no waits and no device-side
-// checks); a kernel with bounded waits would report a timeout nowhere.
+// checks); a kernel with bounded waits would report a timeout nowhere.  The
+// direct-DFT pass kernels, which wait for their streamed twiddle tiles, run
+// only with a plan's tables (g_irows, g_frows), which the plan below leaves
+// null, and the column steps form their twiddles in the kernel without g_cols.
 //
 // Fills both twiddle tables e^{+2 pi i j / N} (double sincospi, rounded once
 // to float) and clears the error word and the debug-flag word after it.  Nothing else in the scratch needs to
