@@ -48,8 +48,24 @@ out["fused_short"] = layer((2, 16, 16, 128, 128, 32, 32))
 out["fused_long_groups"] = layer((1, 4, 4, 512, 512, 16, 16))
 out["generic_fft"] = layer((2, 4, 4, 16, 16, 4, 4))
 out["direct_dft"] = layer((2, 3, 5, 24, 20, 5, 7))
+# the direct-DFT pass kernels: rows of 307 points (every row alignment) and,
+# with 39,040 rows, the residue-class forward rows
+out["direct_dft_passes"] = layer((4, 32, 2, 305, 307, 6, 3))
 out["tensor_memory_3xtf32"] = layer((4, 32, 32, 64, 64, 16, 16), "3xtf32")
 out["single_launch"] = layer((2, 8, 8, 64, 64, 16, 16), single=True)
+
+# the FNO block with the tensor-core pointwise branch (its stores are TMA stores,
+# not range-checked; in this build its shared-memory layout differs)
+shape = B, Cin, Cout, H, W, m1, m2 = (2, 32, 32, 64, 64, 16, 16)
+x, w = rand_layer_inputs(rng, B, Cin, Cout, H, W, m1, m2)
+wpw = (rng.standard_normal((Cout, Cin)) / Cin).astype(np.float32)
+bias = rng.standard_normal(Cout).astype(np.float32)
+plan = fnospec.Plan(*shape)
+y = torch.empty((B, Cout, H, W), device="cuda")
+plan.fno_block_execute(to_dev(x), to_dev(w), to_dev(wpw), to_dev(bias), y)
+torch.cuda.synchronize()
+rel, mx = errors(y.cpu().numpy(), oracle.block(x, f32pairs_to_cplx(w), wpw, bias, m1, m2))
+out["block_tc"] = {"status": plan.fno_get_device_status(), "rel": rel, "max": mx, "plan": "block"}
 
 # the 1D layer (pruned FFT rows and direct DFTs)
 for name, (B, C, L, m) in {"rows1d_fft": (2, 4, 1024, 16), "rows1d_dft": (2, 4, 100, 9)}.items():
