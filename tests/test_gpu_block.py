@@ -26,6 +26,8 @@ BLOCK_CASES = [
     # double-buffered accumulators and y tiles are reused many times
     ((4, 64, 64, 128, 128, 32, 32), "gelu", True),
     ((2, 32, 32, 256, 256, 16, 16), "none", True),
+    ((3, 20, 40, 48, 80, 8, 8), "gelu", False),   # N = 64 with 40 channels: a quarter empty
+    ((17, 16, 16, 8, 8, 2, 2), "gelu", True),     # P = 64 < 128 and 17 units
 ]
 
 

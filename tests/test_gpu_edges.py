@@ -75,6 +75,7 @@ MANY_ROW_SHAPES = [
     (8, 16, 4, 333, 333, 8, 16),
     (4, 32, 2, 305, 307, 6, 3),
     (4, 24, 4, 421, 421, 12, 12),
+    (8, 32, 2, 160, 300, 4, 1),     # one kept column (2 outputs per row), W = 0 mod 4
 ]
 
 
