@@ -22,8 +22,8 @@
 //             buffers;
 //   warps 6-21 epilogue: warp w reads tensor-memory lanes 32 (w mod 4) .. + 31
 //             (pixel rows), quarter (w - 6) / 4 of the accumulator columns, adds
-//             them and the bias to the y tile in
-//             shared memory and applies the activation;
+//             them and the bias to the y tile in shared memory and applies the
+//             activation;
 //   warp 22   y tiles: lane 0 loads the units' y tiles ([Cout][128] floats)
 //             into as many buffers (2 .. 4) as shared memory holds, writes each
 //             finished tile back with a TMA store (pixels past P are not
@@ -110,10 +110,6 @@ __device__ __forceinline__ void split4(float4 v, float4& h, float4& l) {
     h = make_float4(to_tf32(v.x), to_tf32(v.y), to_tf32(v.z), to_tf32(v.w));
     l = make_float4(to_tf32(v.x - h.x), to_tf32(v.y - h.y), to_tf32(v.z - h.z),
                     to_tf32(v.w - h.w));
-}
-
-__device__ __forceinline__ void bulk_wait_read1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 template <int N>
