@@ -28,6 +28,7 @@ BLOCK_CASES = [
     ((2, 32, 32, 256, 256, 16, 16), "none", True),
     ((3, 20, 40, 48, 80, 8, 8), "gelu", False),   # N = 64 with 40 channels: a quarter empty
     ((17, 16, 16, 8, 8, 2, 2), "gelu", True),     # P = 64 < 128 and 17 units
+    ((1, 1, 1, 2, 2, 1, 2), "gelu", True),        # one channel, P = 4: boxes mostly outside
 ]
 
 

@@ -76,6 +76,7 @@ MANY_ROW_SHAPES = [
     (4, 32, 2, 305, 307, 6, 3),
     (4, 24, 4, 421, 421, 12, 12),
     (8, 32, 2, 160, 300, 4, 1),     # one kept column (2 outputs per row), W = 0 mod 4
+    (1, 2, 2, 10, 4000, 2, 30),     # long rows (63 passes), K = 60 of the 64 the pass kernel takes
 ]
 
 
